@@ -1,0 +1,572 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged GQA decode step on GB300.
+
+Headline workload (one "step" = one decode step of a 32-layer model): for each
+of 32 layers, pa_append_kv writes the step's new K/V row of every sequence
+into its page, then pa_decode attends each query head over the 4096 cached
+tokens (paged gather, online softmax, split-K partitions and their exact
+merge).  LLaMA-7B-shaped: batch 8, 32 query = 32 KV heads, head_dim 128, fp16
+KV, page_size 16, one shuffled pool of 65,536 pages.  Synthetic seeded data.
+
+Metric: decode-attention HBM GB/s (algorithmic bytes = unique KV bytes read +
+Q + fp32 output, per (sequence, layer)) and sequences*layers per second.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+path shards by sequence with no data-path collective): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention HBM GB/s and % of GB300 HBM roofline; sequences·layers/sec"
+HEADLINE = "llama7b_b8_ctx4096"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# byte and flop models (per (sequence, layer) call; "吞吐与延迟的系统模型" 4-5)
+
+def decode_bytes(ctx_lens, n_q_heads, n_kv_heads, head_dim, elem_bytes=2):
+    """Unique KV bytes read + Q read + fp32 output written, summed over the
+    sequences of one layer call.  Block tables, the split-K workspace and any
+    re-read are not counted."""
+    kv = sum(2 * int(t) * n_kv_heads * head_dim * elem_bytes for t in ctx_lens)
+    qo = len(ctx_lens) * n_q_heads * head_dim * (elem_bytes + 4)
+    return kv + qo
+
+
+def append_bytes(n_tok, n_kv_heads, head_dim, elem_bytes=2):
+    """K and V rows read from the new-token buffers and written to the pages."""
+    return 2 * 2 * n_tok * n_kv_heads * head_dim * elem_bytes
+
+
+def decode_flops(ctx_lens, n_q_heads, head_dim):
+    """4 * h_q * d * T per sequence: 2 FLOP per multiply-add of q.K^T and P.V."""
+    return sum(4 * n_q_heads * head_dim * int(t) for t in ctx_lens)
+
+
+def prefill_flops(cached, n_new, n_q_heads, head_dim):
+    """Query i sees cached + i + 1 keys; 4 * d FLOP per (query head, key)."""
+    keys = sum(n_new * int(c) + n_new * (n_new + 1) // 2 for c in cached)
+    return 4 * n_q_heads * head_dim * keys
+
+
+def prefill_bytes(cached, n_new, n_q_heads, n_kv_heads, head_dim, elem_bytes=2):
+    kv = sum(2 * (int(c) + n_new) * n_kv_heads * head_dim * elem_bytes for c in cached)
+    qo = len(cached) * n_new * n_q_heads * head_dim * (elem_bytes + 4)
+    return kv + qo
+
+
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def traffic_record(kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (sha256 of the .cu file), else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "paged_kv_cache_171_gb300", "csrc", kernel_file)
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        ent = rec.get(kernel_file)
+        if ent and ent.get("source_sha256") == sha:
+            return ent
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of this GPU's SM clock and throttle reasons."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and parts[0] != self.uuid:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_uuid(torch):
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+def run_headline(torch, pa, workloads, args, rank, world):
+    cfg = workloads.CONFIGS[HEADLINE]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workloads.config_case(HEADLINE, device=dev)
+    L, B = case.layers, case.q.shape[1]
+    hq, hkv, D = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    pages = case.k_cache.shape[0]
+    mb = case.block_table.shape[2]
+    ctx = case.ctx_lens                      # every sequence holds 4096 tokens
+    pos = (ctx - 1).to(torch.int32)          # the step's token is the last one
+    seq_idx = torch.arange(B, dtype=torch.int32, device=dev)
+    k_new, v_new = workloads.new_tokens(L * B, hkv, D, cfg["dtype"], seed=cfg["seed"] + 1,
+                                        device=dev)
+    k_new = k_new.view(L, B, hkv, D)
+    v_new = v_new.view(L, B, hkv, D)
+    out = torch.empty((L, B, hq, D), dtype=torch.float32, device=dev)
+    part = pa.pa_decode_partition_tokens(B, hq, hkv, D, 16, mb, 0)
+    ws_bytes = pa.pa_decode_workspace_size(B, hq, hkv, D, 16, mb, 0)
+    ws = torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device=dev)
+    dcode = case.dtype_code
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    launches_per_layer = 2 + (1 if part else 0)
+
+    def step(ev=None):
+        for layer in range(L):
+            pa.pa_append_kv(k_new[layer], v_new[layer], case.k_cache, case.v_cache,
+                            case.block_table[layer], seq_idx, pos, B, hkv, D, 16, B, mb,
+                            pages, dcode, sptr)
+            if ev is not None:
+                ev[layer][0].record(stream)
+            pa.pa_decode(case.q[layer], case.k_cache, case.v_cache, case.block_table[layer],
+                         ctx, out[layer], case.scale, hq, hkv, D, 16, B, mb, pages, dcode,
+                         0, ws, ws_bytes, sptr)
+            if ev is not None:
+                ev[layer][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert pa.pa_last_device_error() == 0
+
+    ctx_list = [int(t) for t in ctx.cpu()]
+    per_layer_bytes = decode_bytes(ctx_list, hq, hkv, D)
+    step_bytes = L * per_layer_bytes
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_uuid(torch)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(torch, world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for k in range(args.steps):
+        step(ev[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(torch, world)
+    clocks = sampler.stop() if sampler else None
+    status = pa.pa_last_device_error()
+    assert status == 0, pa.pa_strerror(status)
+    ms = t0.elapsed_time(t1)
+    ms_max = allreduce_max(torch, world, ms)
+    call_ms = [ev[k][l][0].elapsed_time(ev[k][l][1]) for k in range(args.steps)
+               for l in range(L)]
+    call_avg_ms = sum(call_ms) / len(call_ms)
+
+    # ---- end to end through the public API with host buffers
+    host_in = {
+        "q": case.q.cpu().pin_memory(),
+        "k_new": k_new.cpu().pin_memory(), "v_new": v_new.cpu().pin_memory(),
+        "block_table": case.block_table.cpu().pin_memory(),
+        "ctx_lens": ctx.cpu().pin_memory(), "pos": pos.cpu().pin_memory(),
+    }
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def step_e2e():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        for layer in range(L):
+            pa.pa_append_kv(dev_in["k_new"][layer], dev_in["v_new"][layer], case.k_cache,
+                            case.v_cache, dev_in["block_table"][layer], seq_idx,
+                            dev_in["pos"], B, hkv, D, 16, B, mb, pages, dcode, sptr)
+            pa.pa_decode(dev_in["q"][layer], case.k_cache, case.v_cache,
+                         dev_in["block_table"][layer], dev_in["ctx_lens"], out[layer],
+                         case.scale, hq, hkv, D, 16, B, mb, pages, dcode, 0, ws, ws_bytes,
+                         sptr)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        step_e2e()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step_e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = allreduce_max(torch, world, e0.elapsed_time(e1))
+    assert pa.pa_last_device_error() == 0
+
+    res = dict(
+        case=case, ms=ms_max, step_bytes=step_bytes, per_layer_bytes=per_layer_bytes,
+        call_avg_ms=call_avg_ms, clocks=clocks, part=part, L=L, B=B,
+        launches=args.steps * L * launches_per_layer,
+        e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ctx_list=ctx_list,
+    )
+    return res
+
+
+def run_other_decode(torch, pa, workloads, name, steps, warmup, partition_tokens=0):
+    """One more decode workload: per step, every layer's pa_decode call."""
+    cfg = workloads.CONFIGS[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workloads.config_case(name, device=dev)
+    L, B = case.layers, case.q.shape[1]
+    hq, hkv, D = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    pages, mb = case.k_cache.shape[0], case.block_table.shape[2]
+    out = torch.empty((L, B, hq, D), dtype=torch.float32, device=dev)
+    ws_bytes = pa.pa_decode_workspace_size(B, hq, hkv, D, 16, mb, partition_tokens)
+    ws = torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device=dev)
+    part = pa.pa_decode_partition_tokens(B, hq, hkv, D, 16, mb, partition_tokens)
+    stream = torch.cuda.current_stream()
+    flush = None
+    ctx_list = [int(t) for t in case.ctx_lens.cpu()]
+    per_layer = decode_bytes(ctx_list, hq, hkv, D)
+    if L * per_layer < 4 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        for layer in range(L):
+            pa.pa_decode(case.q[layer], case.k_cache, case.v_cache, case.block_table[layer],
+                         case.ctx_lens, out[layer], case.scale, hq, hkv, D, 16, B, mb,
+                         pages, case.dtype_code, partition_tokens, ws, ws_bytes,
+                         stream.cuda_stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        if flush is not None:
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    assert pa.pa_last_device_error() == 0
+    ms = statistics.median(times)
+    gbs = L * per_layer / (ms * 1e-3) / 1e9
+    res = {"ms_per_step": round(ms, 4), "GB_s": round(gbs, 1),
+           "seq_layers_per_s": round(L * B / (ms * 1e-3), 1),
+           "partition_tokens": part, "bytes_per_step": L * per_layer,
+           "l2": "flushed (2x L2 write) before each step" if flush is not None
+           else "inputs larger than L2"}
+    del case, out, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_prefill(torch, pa, workloads, steps, warmup, peaks):
+    name = "prefill_b4_512over8192"
+    cfg = workloads.CONFIGS[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workloads.config_case(name, device=dev)
+    B, n_new = case.q.shape[1], case.n_new
+    hq, hkv, D = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    out = torch.empty((B, n_new, hq, D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    cached = [int(t) for t in case.ctx_lens.cpu()]
+    for _ in range(warmup):
+        pa.prefill(case.q[0], case.k_cache, case.v_cache, case.block_table[0],
+                   case.ctx_lens, case.scale, out=out)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pa.prefill(case.q[0], case.k_cache, case.v_cache, case.block_table[0],
+                   case.ctx_lens, case.scale, out=out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    assert pa.pa_last_device_error() == 0
+    ms = statistics.median(times)
+    fl = prefill_flops(cached, n_new, hq, D)
+    tf = fl / (ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops", 1900.0)
+    res = {"ms": round(ms, 4), "TFLOP_s": round(tf, 1), "flops": fl,
+           "frac_of_bf16_peak": round(tf / peak, 4), "peak_tflops": peak,
+           "kernel": "mma.sync m16n8k16 (warp-level tensor cores)",
+           "l2": "flushed (2x L2 write) before each call"}
+    del case, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline_sample(torch, case, cfg, layers_budget_s=10.0):
+    """The float64 oracle, as it stands, on whole layers of the headline
+    workload until ~budget seconds pass (at least one layer)."""
+    import oracle
+    from tests.gpu_support import compact_host_copy  # re-indexing only
+    B = case.q.shape[1]
+    hq, hkv, D = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    threads = oracle.max_threads()
+    done_layers, bytes_done, t_total = 0, 0, 0.0
+    for layer in range(case.layers):
+        q, k, v, table, ctx = compact_host_copy(case, layer, list(range(B)))
+        t = time.perf_counter()
+        oracle.decode(q, k, v, table, ctx, case.scale, case.dtype_code, n_threads=threads)
+        t_total += time.perf_counter() - t
+        done_layers += 1
+        bytes_done += decode_bytes([int(x) for x in ctx], hq, hkv, D)
+        if t_total >= layers_budget_s:
+            break
+    return {"value": round(bytes_done / t_total / 1e9, 3), "unit": "GB/s",
+            "cores": threads, "kind": "oracle",
+            "sample": f"{done_layers} of {case.layers} layers x {B} sequences "
+                      f"(all heads, full 4096-token contexts), float64, OpenMP",
+            "seconds": round(t_total, 2)}
+
+
+# ---------------------------------------------------------------------------
+
+def barrier(torch, world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def allreduce_max(torch, world, x):
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def init_dist(torch, args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def main_ours(args):
+    import torch
+    import paged_kv_cache_171_gb300 as pa
+    from paged_kv_cache_171_gb300 import build as pa_build
+    import workloads
+
+    pa_build.build()
+    rank, world = init_dist(torch, args)
+    peaks, peaks_src = measured_peaks()
+    r = run_headline(torch, pa, workloads, args, rank, world)
+    case = r["case"]
+    ms_step = r["ms"] / args.steps
+    value = world * r["step_bytes"] / (ms_step * 1e-3) / 1e9
+    seq_layers = world * r["L"] * r["B"] / (ms_step * 1e-3)
+    call_gbs = r["per_layer_bytes"] / (r["call_avg_ms"] * 1e-3) / 1e9
+    e2e_ms_step = r["e2e_ms"] / args.steps
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    tr = traffic_record("pa_decode.cu")
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded N(0,1), rounded to fp16)",
+        "config": {
+            "workload": f"{HEADLINE}: decode step of 32 layers x (pa_append_kv + "
+                        "pa_decode), batch 8, 32 q heads / 32 kv heads, head_dim 128, "
+                        "context 4096, fp16 KV, page_size 16, shuffled pool of 65536 "
+                        "pages",
+            "kv_dtype": "fp16", "accumulate": "f32", "out_dtype": "f32",
+            "partition_tokens": r["part"],
+            "l2": "inputs larger than L2 (17.2 GB of KV per step vs 129 MB); no flush",
+            "bytes_per_step": r["step_bytes"],
+        },
+        "seq_layers_per_s": round(seq_layers, 1),
+        "frac_of_hbm_peak": round(value / world / hbm, 4),
+        "roofline": {"bound": "hbm", "achieved": round(call_gbs, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(call_gbs / hbm, 4),
+                     "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                     "peak_source": f"{peaks_src} hbm_gbs (copy)",
+                     "kernel": "pa_decode call (partition kernel + LSE merge)",
+                     "algorithmic_bytes_per_launch": r["per_layer_bytes"],
+                     "avg_launch_ms": round(r["call_avg_ms"], 5)},
+        "e2e": {"value": round(world * r["step_bytes"] / (e2e_ms_step * 1e-3) / 1e9, 1),
+                "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms_step, 4)},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(torch, case, workloads.CONFIGS[HEADLINE])
+    del case, r
+    torch.cuda.empty_cache()
+    if not args.only_headline:
+        other = {}
+        other["gqa4_b64_ragged"] = run_other_decode(torch, pa, workloads,
+                                                    "gqa4_b64_ragged", 5, 3)
+        other["gqa8_b4_ctx32k"] = run_other_decode(torch, pa, workloads,
+                                                   "gqa8_b4_ctx32k", 20, 5, 512)
+        other["mha_b1_ctx512"] = run_other_decode(torch, pa, workloads,
+                                                  "mha_b1_ctx512", 20, 5)
+        other["prefill_b4_512over8192"] = run_prefill(torch, pa, workloads, 10, 3, peaks)
+        for k, v in other.items():
+            if "GB_s" in v:
+                v["frac_of_hbm_peak"] = round(v["GB_s"] / hbm, 4)
+        line["other_workloads"] = other
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main_reference(args):
+    """The float64 oracle as the reference arm, on the host cores."""
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    import workloads
+    oracle.build.build() if hasattr(oracle, "build") else None
+    cfg = workloads.CONFIGS[HEADLINE]
+    # the same workload, built on the host; each step = one whole layer
+    # (8 sequences x 32 heads x 4096 tokens) through the oracle
+    B, hq, hkv, D = cfg["batch"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    case = workloads.paged_case(**{**cfg, "layers": 1, "pool_pages": None})
+    threads = oracle.max_threads()
+    ctx = [int(t) for t in case.ctx_lens]
+    per_layer = decode_bytes(ctx, hq, hkv, D)
+
+    def step():
+        oracle.decode(case.q[0], case.k_cache, case.v_cache, case.block_table[0],
+                      case.ctx_lens, case.scale, case.dtype_code, n_threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    sec = time.perf_counter() - t
+    ms = sec * 1e3 / args.steps
+    gbs = per_layer / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), fp16)",
+        "config": {"workload": f"{HEADLINE}: one layer (8 sequences x 32 heads x 4096 "
+                               "tokens) of the decode step per step, float64 oracle"},
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": "one of 32 layers per step (the oracle's decode)"},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only-headline", action="store_true",
+                    help="skip the other workloads (ragged GQA, 32k split-K, prefill)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        main_reference(args)
+    else:
+        main_ours(args)
+
+
+if __name__ == "__main__":
+    main()

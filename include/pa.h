@@ -1,0 +1,196 @@
+/*
+ * pa.h -- C ABI of libpa, paged GQA attention for GB300 (sm_103a).
+ *
+ * Every entry point takes plain pointers and sizes.  Device pointers are
+ * marked "device"; they must point into memory of the current CUDA device.
+ * The caller owns every buffer.  The library allocates no device memory,
+ * never synchronises a stream (except pa_last_device_error, which says so),
+ * and queues its kernels on `stream` (NULL = the legacy default stream).
+ *
+ * Return value of every int entry point: PA_OK (0), or a negative PA_ERR_*
+ * code when an argument is invalid -- in that case nothing was launched --
+ * or PA_ERR_CUDA when a launch failed.  Data-dependent errors that only the
+ * GPU can see (a block-table entry outside the pool, a context length out of
+ * range, a wait that ran out) do not fault: the kernel skips the bad access,
+ * records the first such error in a device status word, and carries on;
+ * pa_last_device_error() reads and clears it.
+ *
+ * Cache layout (the pages do not fix one; this is the library's choice):
+ *   k_cache, v_cache: [num_pages][n_kv_heads][page_size][head_dim] elements,
+ *   so one (page, kv head) tile of page_size rows is one contiguous block.
+ * Logical token t of sequence b lives in physical page
+ *   block_table[b * max_blocks_per_seq + t / page_size], slot t % page_size
+ * (PagedAttention's block table: ch. 19 "推理系统与性能工程", 19.7.3).
+ * Query head h reads KV head h / (n_q_heads / n_kv_heads): contiguous GQA
+ * groups ("吞吐与延迟的系统模型", sections 4-5: several query heads share one
+ * KV head; the grouping order is our reading).
+ *
+ * Supported: head_dim 64 or 128, page_size 16 (the block size whose internal
+ * fragmentation is at most 15 token slots, 19.7.3), n_q_heads a multiple of
+ * n_kv_heads, bf16 or fp16 Q/K/V, fp32 output and accumulation.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so this header needs no CUDA
+ * include. */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum { PA_BF16 = 0, PA_F16 = 1 } pa_dtype;
+
+enum {
+  PA_OK = 0,
+  PA_ERR_NULL = -1,        /* a required pointer is NULL */
+  PA_ERR_HEADS = -2,       /* heads <= 0 or n_q_heads % n_kv_heads != 0 */
+  PA_ERR_HEAD_DIM = -3,    /* head_dim not 64 or 128 */
+  PA_ERR_PAGE_SIZE = -4,   /* page_size not 16 */
+  PA_ERR_SHAPE = -5,       /* batch, max_blocks_per_seq, num_pages, n_tok or
+                              n_new negative/zero where not allowed, or too big */
+  PA_ERR_DTYPE = -6,       /* dtype not PA_BF16 / PA_F16 */
+  PA_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than required */
+  PA_ERR_ALIGN = -8,       /* a pointer not 16-byte aligned */
+  PA_ERR_PARTITION = -9,   /* partition_tokens not 0 and not a positive
+                              multiple of page_size */
+  PA_ERR_CUDA = -10,       /* a CUDA runtime call or launch failed */
+  PA_ERR_BAD_BLOCK = -11,  /* device: block-table entry outside [0, num_pages) */
+  PA_ERR_BAD_CTX = -12,    /* device: context length < 0 or beyond the table */
+  PA_ERR_TIMEOUT = -13,    /* device: a bounded wait for a copy ran out */
+  PA_ERR_BAD_INDEX = -14   /* device: append seq_idx / pos outside the table */
+};
+
+/* Human-readable name of a status code.  Never NULL. */
+const char *pa_strerror(int status);
+
+/*
+ * pa_decode -- decode-step attention over the paged cache.
+ *
+ * For every sequence b and query head h, with g = h / G, G = n_q_heads /
+ * n_kv_heads and T = ctx_lens[b]:
+ *   s_t = scale * <q[b][h], k_t>            t = 0 .. T-1, k_t = K row of token t
+ *   out[b][h] = sum_t e^(s_t - m) v_t / sum_t e^(s_t - m),   m = max_t s_t
+ * i.e. o = softmax(q K^T * scale) V (ch. 19 "推理系统与性能工程", 19.4.1 and the
+ * stable softmax of 19.6.2).  It is evaluated page by page with the online
+ * recurrence of 19.6.2 (running max m, running sum l, unnormalised O); one
+ * K/V page read serves all G query heads of its group.  Long contexts are
+ * cut into partitions of `partition_tokens` tokens whose partial states
+ * (m_p, l_p, O_p) are merged exactly (the exponent law of 19.6.2) by a second
+ * kernel.  T = 0 writes zeros.
+ *
+ *   q            device, [batch][n_q_heads][head_dim], dtype
+ *   k_cache      device, [num_pages][n_kv_heads][page_size][head_dim], dtype
+ *   v_cache      device, same shape
+ *   block_table  device int32 [batch][max_blocks_per_seq]; only the first
+ *                ceil(T/page_size) entries of row b are read
+ *   ctx_lens     device int32 [batch], 0 <= T <= max_blocks_per_seq*page_size
+ *   out          device float [batch][n_q_heads][head_dim]
+ *   scale        softmax scale, applied before the max (1/sqrt(head_dim) in
+ *                the pages' formula)
+ *   partition_tokens  0 = choose automatically; otherwise a multiple of
+ *                page_size: every sequence is processed in chunks of that
+ *                many tokens and merged
+ *   workspace    device, >= pa_decode_workspace_size(...) bytes, 16-byte
+ *                aligned; may be NULL when that size is 0.  Holds the
+ *                partial states; contents on entry do not matter.
+ * q, k_cache, v_cache, out and workspace must be 16-byte aligned.
+ */
+int pa_decode(const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_table, const int32_t *ctx_lens, float *out,
+              float scale, int n_q_heads, int n_kv_heads, int head_dim,
+              int page_size, int batch, int max_blocks_per_seq, int num_pages,
+              pa_dtype dtype, int partition_tokens, void *workspace,
+              size_t workspace_bytes, pa_stream_t stream);
+
+/* The partition size pa_decode would use (0 = a single pass, no workspace)
+ * for these arguments and partition_tokens (0 = automatic), on the current
+ * device.  Returns a negative PA_ERR_* on invalid arguments. */
+int pa_decode_partition_tokens(int batch, int n_q_heads, int n_kv_heads,
+                               int head_dim, int page_size,
+                               int max_blocks_per_seq, int partition_tokens);
+
+/* Workspace bytes pa_decode needs for the same arguments (0 when it runs in a
+ * single pass).  Layout: float [batch][n_q_heads][n_parts][head_dim + 2],
+ * each row (O_p[0..head_dim-1], m_p, l_p) with m_p in natural-log units. */
+size_t pa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                int head_dim, int page_size,
+                                int max_blocks_per_seq, int partition_tokens);
+
+/*
+ * pa_merge_partials -- the exact merge of partition states on its own.
+ *
+ * For row (b, h) with n = ceil(ctx_lens[b] / partition_tokens) valid parts
+ * p < n (parts at p >= n are not read):
+ *   M = max_p m_p,  l = sum_p e^(m_p - M) l_p,  out = sum_p e^(m_p - M) O_p / l
+ * (the exponent law e^(a+b) = e^a e^b of ch. 19 19.6.2, applied to two
+ * summarised chunks).  A part with l_p = 0 contributes nothing; a row with
+ * none writes zeros.
+ *   partials  device float [batch][n_q_heads][n_parts][head_dim + 2]
+ *   out       device float [batch][n_q_heads][head_dim]
+ */
+int pa_merge_partials(const float *partials, const int32_t *ctx_lens,
+                      float *out, int batch, int n_q_heads, int head_dim,
+                      int n_parts, int partition_tokens, pa_stream_t stream);
+
+/*
+ * pa_append_kv -- write the K and V rows of new tokens into their pages.
+ *
+ * Token j (0 <= j < n_tok) belongs to sequence seq_idx[j] at logical position
+ * pos[j]; for every kv head its rows k_new[j][g], v_new[j][g] are stored at
+ * page block_table[seq_idx[j]][pos[j] / page_size], slot pos[j] % page_size.
+ * This is the new-KV write of a decode step ("吞吐与延迟的系统模型", section 4:
+ * 2LBd_kv b_kv bytes written per step).  The block table must already map
+ * the position's block (allocating pages is the caller's business).
+ *   k_new, v_new  device, [n_tok][n_kv_heads][head_dim], dtype, 16-B aligned
+ *   k_cache, v_cache  device, written in place
+ *   seq_idx, pos  device int32 [n_tok]
+ * Two tokens must not target the same (page, slot): the order of such writes
+ * is unspecified.  A bad seq_idx/pos/page skips that token and records
+ * PA_ERR_BAD_INDEX / PA_ERR_BAD_BLOCK.
+ */
+int pa_append_kv(const void *k_new, const void *v_new, void *k_cache,
+                 void *v_cache, const int32_t *block_table,
+                 const int32_t *seq_idx, const int32_t *pos, int n_tok,
+                 int n_kv_heads, int head_dim, int page_size, int batch,
+                 int max_blocks_per_seq, int num_pages, pa_dtype dtype,
+                 pa_stream_t stream);
+
+/*
+ * pa_prefill_paged -- chunked-prefill attention of n_new new query tokens per
+ * sequence over the paged cache, causal.
+ *
+ * ctx_lens[b] counts tokens cached before the chunk; the chunk's own K/V rows
+ * must already be stored (e.g. by pa_append_kv) at positions ctx_lens[b] ..
+ * ctx_lens[b] + n_new - 1.  Query i of sequence b attends keys
+ * 0 .. ctx_lens[b] + i (prefill over the cache, ch. 19 19.3.1; tiled as the
+ * FlashAttention forward of 19.6.3 with the online recurrence of 19.6.2).
+ *   q    device, [batch][n_new][n_q_heads][head_dim], dtype
+ *   out  device float [batch][n_new][n_q_heads][head_dim]
+ * Same cache, table and head arguments as pa_decode.
+ */
+int pa_prefill_paged(const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, const int32_t *ctx_lens,
+                     int n_new, float *out, float scale, int n_q_heads,
+                     int n_kv_heads, int head_dim, int page_size, int batch,
+                     int max_blocks_per_seq, int num_pages, pa_dtype dtype,
+                     pa_stream_t stream);
+
+/*
+ * pa_last_device_error -- synchronise `stream`, then return and clear the
+ * device status word (PA_OK if no kernel recorded an error since the last
+ * call).  The word is shared by every stream of the device: it reports the
+ * first error any pa kernel recorded.  Returns PA_ERR_CUDA if the stream
+ * itself reports a CUDA error.
+ */
+int pa_last_device_error(pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

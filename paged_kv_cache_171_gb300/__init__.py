@@ -1,0 +1,216 @@
+"""paged_kv_cache_171_gb300 -- paged GQA attention for GB300 (sm_103a).
+
+A thin ctypes binding over libpa.so, whose C ABI is include/pa.h.  The
+functions named like the C entry points (``pa_decode``, ``pa_append_kv``,
+``pa_prefill_paged``, ``pa_merge_partials``, ...) only marshal arguments:
+torch tensors become device pointers, the stream becomes a cudaStream_t,
+and a nonzero status raises :class:`PAError`.  Every step of the attention
+runs in libpa's CUDA kernels; there is no CPU or PyTorch fallback, and using
+any of these functions without a built libpa.so raises.
+
+Build the library with ``python -m paged_kv_cache_171_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "PAError", "BF16", "F16", "lib", "dtype_code", "pa_decode",
+    "pa_decode_partition_tokens", "pa_decode_workspace_size",
+    "pa_merge_partials", "pa_append_kv", "pa_prefill_paged",
+    "pa_last_device_error", "pa_strerror", "decode", "prefill", "append_kv",
+]
+
+BF16 = 0
+F16 = 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libpa.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "pa.h")
+
+_lib = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {pa_strerror(status)} ({status})")
+
+
+def lib():
+    """The loaded libpa.so (ctypes.CDLL); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"libpa.so not built ({LIB_PATH}); run "
+                "`python -m paged_kv_cache_171_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.pa_strerror.argtypes = [I]
+        L.pa_strerror.restype = ctypes.c_char_p
+        L.pa_decode.argtypes = [P, P, P, P, P, P, F] + [I] * 8 + [I, P, Z, P]
+        L.pa_decode.restype = I
+        L.pa_decode_partition_tokens.argtypes = [I] * 7
+        L.pa_decode_partition_tokens.restype = I
+        L.pa_decode_workspace_size.argtypes = [I] * 7
+        L.pa_decode_workspace_size.restype = Z
+        L.pa_merge_partials.argtypes = [P, P, P, I, I, I, I, I, P]
+        L.pa_merge_partials.restype = I
+        L.pa_append_kv.argtypes = [P] * 7 + [I] * 8 + [P]
+        L.pa_append_kv.restype = I
+        L.pa_prefill_paged.argtypes = [P, P, P, P, P, I, P, F] + [I] * 8 + [P]
+        L.pa_prefill_paged.restype = I
+        L.pa_last_device_error.argtypes = [P]
+        L.pa_last_device_error.restype = I
+        _lib = L
+    return _lib
+
+
+def pa_strerror(status: int) -> str:
+    try:
+        return lib().pa_strerror(int(status)).decode()
+    except ImportError:
+        return f"status {status}"
+
+
+def dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float16:
+        return F16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != 0:
+        raise PAError(rc, where)
+    return rc
+
+
+# --- the C entry points, same names and argument order ------------------------
+
+def pa_decode(q, k_cache, v_cache, block_table, ctx_lens, out, scale, n_q_heads,
+              n_kv_heads, head_dim, page_size, batch, max_blocks_per_seq,
+              num_pages, dtype, partition_tokens=0, workspace=None,
+              workspace_bytes=0, stream=None) -> int:
+    rc = lib().pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                         _ptr(ctx_lens), _ptr(out), float(scale), n_q_heads,
+                         n_kv_heads, head_dim, page_size, batch,
+                         max_blocks_per_seq, num_pages, dtype, partition_tokens,
+                         _ptr(workspace), workspace_bytes, _stream(stream))
+    return _check(rc, "pa_decode")
+
+
+def pa_decode_partition_tokens(batch, n_q_heads, n_kv_heads, head_dim, page_size,
+                               max_blocks_per_seq, partition_tokens=0) -> int:
+    rc = lib().pa_decode_partition_tokens(batch, n_q_heads, n_kv_heads, head_dim,
+                                          page_size, max_blocks_per_seq,
+                                          partition_tokens)
+    if rc < 0:
+        raise PAError(rc, "pa_decode_partition_tokens")
+    return rc
+
+
+def pa_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, page_size,
+                             max_blocks_per_seq, partition_tokens=0) -> int:
+    return lib().pa_decode_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+                                          page_size, max_blocks_per_seq,
+                                          partition_tokens)
+
+
+def pa_merge_partials(partials, ctx_lens, out, batch, n_q_heads, head_dim,
+                      n_parts, partition_tokens, stream=None) -> int:
+    rc = lib().pa_merge_partials(_ptr(partials), _ptr(ctx_lens), _ptr(out), batch,
+                                 n_q_heads, head_dim, n_parts, partition_tokens,
+                                 _stream(stream))
+    return _check(rc, "pa_merge_partials")
+
+
+def pa_append_kv(k_new, v_new, k_cache, v_cache, block_table, seq_idx, pos, n_tok,
+                 n_kv_heads, head_dim, page_size, batch, max_blocks_per_seq,
+                 num_pages, dtype, stream=None) -> int:
+    rc = lib().pa_append_kv(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                            _ptr(block_table), _ptr(seq_idx), _ptr(pos), n_tok,
+                            n_kv_heads, head_dim, page_size, batch,
+                            max_blocks_per_seq, num_pages, dtype, _stream(stream))
+    return _check(rc, "pa_append_kv")
+
+
+def pa_prefill_paged(q, k_cache, v_cache, block_table, ctx_lens, n_new, out, scale,
+                     n_q_heads, n_kv_heads, head_dim, page_size, batch,
+                     max_blocks_per_seq, num_pages, dtype, stream=None) -> int:
+    rc = lib().pa_prefill_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(block_table), _ptr(ctx_lens), n_new, _ptr(out),
+                                float(scale), n_q_heads, n_kv_heads, head_dim,
+                                page_size, batch, max_blocks_per_seq, num_pages,
+                                dtype, _stream(stream))
+    return _check(rc, "pa_prefill_paged")
+
+
+def pa_last_device_error(stream=None) -> int:
+    """Synchronises the stream; returns and clears the device status word."""
+    return lib().pa_last_device_error(_stream(stream))
+
+
+# --- tensor-shaped conveniences (allocation by torch, compute by libpa) ------
+
+def decode(q, k_cache, v_cache, block_table, ctx_lens, scale, partition_tokens=0,
+           out=None, workspace=None, stream=None):
+    """q [B, h_q, D]; caches [pages, h_kv, 16, D]; block_table int32 [B, max_blocks];
+    ctx_lens int32 [B].  Returns fp32 [B, h_q, D]."""
+    import torch
+    B, hq, D = q.shape
+    pages, hkv, P, D2 = k_cache.shape
+    assert D2 == D and block_table.shape[0] == B
+    mb = block_table.shape[1]
+    if out is None:
+        out = torch.empty((B, hq, D), dtype=torch.float32, device=q.device)
+    ws_bytes = pa_decode_workspace_size(B, hq, hkv, D, P, mb, partition_tokens)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=q.device)
+    pa_decode(q, k_cache, v_cache, block_table, ctx_lens, out, scale, hq, hkv, D, P,
+              B, mb, pages, dtype_code(q), partition_tokens, workspace,
+              ws_bytes, stream)
+    return out
+
+
+def append_kv(k_new, v_new, k_cache, v_cache, block_table, seq_idx, pos, stream=None):
+    n_tok, hkv, D = k_new.shape
+    pages, _, P, _ = k_cache.shape
+    B, mb = block_table.shape
+    pa_append_kv(k_new, v_new, k_cache, v_cache, block_table, seq_idx, pos, n_tok,
+                 hkv, D, P, B, mb, pages, dtype_code(k_new), stream)
+
+
+def prefill(q, k_cache, v_cache, block_table, ctx_lens, scale, out=None, stream=None):
+    """q [B, n_new, h_q, D]; ctx_lens = cached tokens before the chunk."""
+    import torch
+    B, n_new, hq, D = q.shape
+    pages, hkv, P, _ = k_cache.shape
+    mb = block_table.shape[1]
+    if out is None:
+        out = torch.empty((B, n_new, hq, D), dtype=torch.float32, device=q.device)
+    pa_prefill_paged(q, k_cache, v_cache, block_table, ctx_lens, n_new, out, scale,
+                     hq, hkv, D, P, B, mb, pages, dtype_code(q), stream)
+    return out

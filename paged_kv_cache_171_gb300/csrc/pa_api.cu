@@ -1,0 +1,378 @@
+// pa_api.cu -- the C ABI of libpa: argument validation, dispatch, the device
+// status word, tensor-map encoding, and the KV-append kernel.
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// One status word per device: the first data-dependent error any kernel saw.
+__device__ int g_status_word;
+
+int *device_status(int device) {
+  static std::mutex mu;
+  static int *addr[64] = {};
+  if (device < 0 || device >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[device]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    addr[device] = static_cast<int *>(p);
+  }
+  return addr[device];
+}
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                   void *, const cuuint64_t *, const cuuint64_t *,
+                                   const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+int make_rows_map(CUtensorMap *map, const void *base, uint64_t rows,
+                  int head_dim, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+namespace {
+
+// ---- KV append: one thread moves 16 bytes of K and 16 bytes of V
+__global__ void __launch_bounds__(256)
+    append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                  uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                  const int32_t *__restrict__ block_table,
+                  const int32_t *__restrict__ seq_idx,
+                  const int32_t *__restrict__ pos, int *status, long total,
+                  int n_kv_heads, int chunks, int batch, int max_blocks,
+                  int num_pages) {
+  const long idx = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const int c = static_cast<int>(idx % chunks);
+  const long jg = idx / chunks;
+  const int g = static_cast<int>(jg % n_kv_heads);
+  const long j = jg / n_kv_heads;
+  const bool reporter = (c == 0 && g == 0);
+  const int b = seq_idx[j];
+  const int t = pos[j];
+  if (b < 0 || b >= batch || t < 0 || t >= max_blocks * kPageSize) {
+    if (reporter) record_error(status, PA_ERR_BAD_INDEX);
+    return;
+  }
+  const int page = block_table[static_cast<size_t>(b) * max_blocks + t / kPageSize];
+  if (page < 0 || page >= num_pages) {
+    if (reporter) record_error(status, PA_ERR_BAD_BLOCK);
+    return;
+  }
+  const size_t dst =
+      ((static_cast<size_t>(page) * n_kv_heads + g) * kPageSize + t % kPageSize) *
+          chunks + c;
+  const size_t src = static_cast<size_t>(jg) * chunks + c;
+  k_cache[dst] = k_new[src];
+  v_cache[dst] = v_new[src];
+}
+
+}  // namespace
+
+int launch_append(const void *k_new, const void *v_new, void *k_cache,
+                  void *v_cache, const int32_t *block_table,
+                  const int32_t *seq_idx, const int32_t *pos, int *status,
+                  int n_tok, int n_kv_heads, int head_dim, int batch,
+                  int max_blocks, int num_pages, cudaStream_t stream) {
+  const int chunks = head_dim / 8;  // 16-byte chunks per row
+  const long total = static_cast<long>(n_tok) * n_kv_heads * chunks;
+  const int threads = 256;
+  const long blocks = (total + threads - 1) / threads;
+  append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), block_table,
+      seq_idx, pos, status, total, n_kv_heads, chunks, batch, max_blocks,
+      num_pages);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_common(int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                 int batch, int max_blocks, int num_pages, int dtype) {
+  if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return PA_ERR_HEADS;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_HEAD_DIM;
+  if (page_size != kPageSize) return PA_ERR_PAGE_SIZE;
+  if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_DTYPE;
+  if (batch <= 0 || batch > 65535 || max_blocks <= 0 || num_pages <= 0)
+    return PA_ERR_SHAPE;
+  // Token positions and TMA row coordinates are 32-bit.
+  if (static_cast<int64_t>(max_blocks) * page_size > (int64_t(1) << 30)) return PA_ERR_SHAPE;
+  if (static_cast<int64_t>(num_pages) * n_kv_heads * page_size >= (int64_t(1) << 31))
+    return PA_ERR_SHAPE;
+  return PA_OK;
+}
+
+int current_status_ptr(int **status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  *status = device_status(dev);
+  return *status ? PA_OK : PA_ERR_CUDA;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+// Partition plan of pa_decode: pages per partition (0 = single pass) and the
+// partition count.  Automatic mode cuts sequences so that the grid holds a
+// few waves of resident CTAs even when batch * heads is small, and so that
+// one long sequence cannot make a tail of its own.
+int decode_plan(int batch, int n_q_heads, int n_kv_heads, int max_blocks,
+                int partition_tokens, int *part_pages, int *n_parts) {
+  if (partition_tokens < 0 || partition_tokens % kPageSize) return PA_ERR_PARTITION;
+  int pp = partition_tokens / kPageSize;
+  if (pp == 0) {
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    const int64_t resident = static_cast<int64_t>(sms) * 2;  // CTAs per SM
+    const int64_t items = static_cast<int64_t>(batch) * n_kv_heads *
+                          ((n_q_heads / n_kv_heads) / group_tile(n_q_heads / n_kv_heads));
+    // aim for ~8 partition-sized CTAs per resident slot if every sequence were
+    // full-length, but never cut below 16 pages (256 tokens)
+    int64_t target = (items * max_blocks + resident * 8 - 1) / (resident * 8);
+    if (target < 16) target = 16;
+    if (target >= max_blocks) {
+      pp = 0;
+    } else {
+      const int64_t np = (max_blocks + target - 1) / target;
+      pp = static_cast<int>((max_blocks + np - 1) / np);  // equal-sized parts
+    }
+  }
+  if (pp >= max_blocks) pp = 0;
+  *part_pages = pp;
+  *n_parts = pp ? (max_blocks + pp - 1) / pp : 1;
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char *pa_strerror(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_NULL: return "PA_ERR_NULL: a required pointer is NULL";
+    case PA_ERR_HEADS: return "PA_ERR_HEADS: bad head counts";
+    case PA_ERR_HEAD_DIM: return "PA_ERR_HEAD_DIM: head_dim must be 64 or 128";
+    case PA_ERR_PAGE_SIZE: return "PA_ERR_PAGE_SIZE: page_size must be 16";
+    case PA_ERR_SHAPE: return "PA_ERR_SHAPE: bad or too large sizes";
+    case PA_ERR_DTYPE: return "PA_ERR_DTYPE: dtype must be PA_BF16 or PA_F16";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_ALIGN: return "PA_ERR_ALIGN: pointer not 16-byte aligned";
+    case PA_ERR_PARTITION: return "PA_ERR_PARTITION: partition_tokens not a multiple of page_size";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: a CUDA call failed";
+    case PA_ERR_BAD_BLOCK: return "PA_ERR_BAD_BLOCK: block-table entry outside the page pool";
+    case PA_ERR_BAD_CTX: return "PA_ERR_BAD_CTX: context length outside [0, max_blocks*page_size]";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded wait for a copy ran out";
+    case PA_ERR_BAD_INDEX: return "PA_ERR_BAD_INDEX: append seq_idx/pos outside the table";
+    default: return "unknown pa status";
+  }
+}
+
+int pa_decode_partition_tokens(int batch, int n_q_heads, int n_kv_heads,
+                               int head_dim, int page_size,
+                               int max_blocks_per_seq, int partition_tokens) {
+  int rc = check_common(n_q_heads, n_kv_heads, head_dim, page_size, batch,
+                        max_blocks_per_seq, 1, PA_BF16);
+  if (rc) return rc;
+  int pp = 0, np = 1;
+  rc = decode_plan(batch, n_q_heads, n_kv_heads, max_blocks_per_seq,
+                   partition_tokens, &pp, &np);
+  return rc ? rc : pp * kPageSize;
+}
+
+size_t pa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                int head_dim, int page_size,
+                                int max_blocks_per_seq, int partition_tokens) {
+  if (check_common(n_q_heads, n_kv_heads, head_dim, page_size, batch,
+                   max_blocks_per_seq, 1, PA_BF16))
+    return 0;
+  int pp = 0, np = 1;
+  if (decode_plan(batch, n_q_heads, n_kv_heads, max_blocks_per_seq,
+                  partition_tokens, &pp, &np))
+    return 0;
+  if (np <= 1) return 0;
+  return static_cast<size_t>(batch) * n_q_heads * np * (head_dim + 2) * sizeof(float);
+}
+
+int pa_decode(const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_table, const int32_t *ctx_lens, float *out,
+              float scale, int n_q_heads, int n_kv_heads, int head_dim,
+              int page_size, int batch, int max_blocks_per_seq, int num_pages,
+              pa_dtype dtype, int partition_tokens, void *workspace,
+              size_t workspace_bytes, pa_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !out)
+    return PA_ERR_NULL;
+  int rc = check_common(n_q_heads, n_kv_heads, head_dim, page_size, batch,
+                        max_blocks_per_seq, num_pages, dtype);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_ALIGN;
+  int pp = 0, np = 1;
+  rc = decode_plan(batch, n_q_heads, n_kv_heads, max_blocks_per_seq,
+                   partition_tokens, &pp, &np);
+  if (rc) return rc;
+  if (np > 1) {
+    const size_t need =
+        static_cast<size_t>(batch) * n_q_heads * np * (head_dim + 2) * sizeof(float);
+    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_ALIGN;
+  }
+  DecodeLaunch a;
+  rc = current_status_ptr(&a.status);
+  if (rc) return rc;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.ctx_lens = ctx_lens;
+  a.out = out;
+  a.workspace = np > 1 ? static_cast<float *>(workspace) : nullptr;
+  a.scale = scale;
+  a.n_q_heads = n_q_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.head_dim = head_dim;
+  a.batch = batch;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_pages = num_pages;
+  a.bf16 = dtype == PA_BF16;
+  a.part_pages = pp;
+  a.n_parts = np;
+  return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_merge_partials(const float *partials, const int32_t *ctx_lens,
+                      float *out, int batch, int n_q_heads, int head_dim,
+                      int n_parts, int partition_tokens, pa_stream_t stream) {
+  if (!partials || !ctx_lens || !out) return PA_ERR_NULL;
+  if (n_q_heads <= 0) return PA_ERR_HEADS;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_HEAD_DIM;
+  if (batch <= 0 || batch > 65535 || n_q_heads > 65535 || n_parts <= 0)
+    return PA_ERR_SHAPE;
+  if (partition_tokens <= 0) return PA_ERR_PARTITION;
+  int *status = nullptr;
+  int rc = current_status_ptr(&status);
+  if (rc) return rc;
+  return launch_merge(partials, ctx_lens, out, status, batch, n_q_heads,
+                      head_dim, n_parts, partition_tokens,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_append_kv(const void *k_new, const void *v_new, void *k_cache,
+                 void *v_cache, const int32_t *block_table,
+                 const int32_t *seq_idx, const int32_t *pos, int n_tok,
+                 int n_kv_heads, int head_dim, int page_size, int batch,
+                 int max_blocks_per_seq, int num_pages, pa_dtype dtype,
+                 pa_stream_t stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !seq_idx || !pos)
+    return PA_ERR_NULL;
+  int rc = check_common(n_kv_heads, n_kv_heads, head_dim, page_size, batch,
+                        max_blocks_per_seq, num_pages, dtype);
+  if (rc) return rc;
+  if (n_tok < 0) return PA_ERR_SHAPE;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_ALIGN;
+  if (n_tok == 0) return PA_OK;
+  int *status = nullptr;
+  rc = current_status_ptr(&status);
+  if (rc) return rc;
+  return launch_append(k_new, v_new, k_cache, v_cache, block_table, seq_idx, pos,
+                       status, n_tok, n_kv_heads, head_dim, batch,
+                       max_blocks_per_seq, num_pages,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_prefill_paged(const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, const int32_t *ctx_lens,
+                     int n_new, float *out, float scale, int n_q_heads,
+                     int n_kv_heads, int head_dim, int page_size, int batch,
+                     int max_blocks_per_seq, int num_pages, pa_dtype dtype,
+                     pa_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !out)
+    return PA_ERR_NULL;
+  int rc = check_common(n_q_heads, n_kv_heads, head_dim, page_size, batch,
+                        max_blocks_per_seq, num_pages, dtype);
+  if (rc) return rc;
+  if (n_new < 0 || n_new > (1 << 20)) return PA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_ALIGN;
+  if (n_new == 0) return PA_OK;
+  PrefillLaunch a;
+  rc = current_status_ptr(&a.status);
+  if (rc) return rc;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.ctx_lens = ctx_lens;
+  a.out = out;
+  a.scale = scale;
+  a.n_new = n_new;
+  a.n_q_heads = n_q_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.head_dim = head_dim;
+  a.batch = batch;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_pages = num_pages;
+  a.bf16 = dtype == PA_BF16;
+  return launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_last_device_error(pa_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  int *status = nullptr;
+  if (current_status_ptr(&status)) return PA_ERR_CUDA;
+  int value = 0;
+  const int zero = 0;
+  if (cudaMemcpyAsync(&value, status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaMemcpyAsync(status, &zero, sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  return value;
+}
+
+}  // extern "C"

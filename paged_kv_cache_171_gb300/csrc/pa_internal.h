@@ -1,0 +1,73 @@
+// pa_internal.h -- host-side interfaces between the C-ABI layer (pa_api.cu)
+// and the translation units that hold the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+constexpr int kPageSize = 16;  // tokens per page (the only one supported)
+
+// Everything the decode kernels need, already validated by pa_api.cu.
+struct DecodeLaunch {
+  const void *q;
+  const void *k_cache;
+  const void *v_cache;
+  const int32_t *block_table;
+  const int32_t *ctx_lens;
+  float *out;
+  float *workspace;  // partial states, or nullptr for a single pass
+  int *status;
+  float scale;
+  int n_q_heads, n_kv_heads, head_dim, batch, max_blocks, num_pages;
+  bool bf16;
+  int part_pages;  // pages per partition; 0 = a single pass over the sequence
+  int n_parts;     // partitions per sequence (1 for a single pass)
+};
+
+int launch_decode(const DecodeLaunch &a, cudaStream_t stream);
+
+int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,
+                 int *status, int batch, int n_q_heads, int head_dim,
+                 int n_parts, int partition_tokens, cudaStream_t stream);
+
+int launch_append(const void *k_new, const void *v_new, void *k_cache,
+                  void *v_cache, const int32_t *block_table,
+                  const int32_t *seq_idx, const int32_t *pos, int *status,
+                  int n_tok, int n_kv_heads, int head_dim, int batch,
+                  int max_blocks, int num_pages, cudaStream_t stream);
+
+struct PrefillLaunch {
+  const void *q;
+  const void *k_cache;
+  const void *v_cache;
+  const int32_t *block_table;
+  const int32_t *ctx_lens;
+  float *out;
+  int *status;
+  float scale;
+  int n_new, n_q_heads, n_kv_heads, head_dim, batch, max_blocks, num_pages;
+  bool bf16;
+};
+
+int launch_prefill(const PrefillLaunch &a, cudaStream_t stream);
+
+// Device address of this device's status word (looked up once per device).
+int *device_status(int device);
+
+// Tiled tensor map over a [rows][head_dim] 16-bit matrix, box {64, box_rows},
+// 128-byte swizzle.  Returns PA_OK or PA_ERR_CUDA.
+int make_rows_map(CUtensorMap *map, const void *base, uint64_t rows,
+                  int head_dim, int box_rows);
+
+// Largest group tile (heads handled by one CTA) that divides the group size.
+inline int group_tile(int group) {
+  return (group % 8 == 0) ? 8 : (group % 4 == 0) ? 4 : (group % 2 == 0) ? 2 : 1;
+}
+
+}  // namespace pa

@@ -1,0 +1,133 @@
+"""libpa.so loads, exports every entry point include/pa.h declares, and rejects
+invalid arguments on the host before touching a GPU (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_171_gb300 as pa
+from paged_kv_cache_171_gb300 import build as pa_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    pa_build.build()
+    return pa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("pa_decode", "pa_append_kv", "pa_prefill_paged",
+                 "pa_merge_partials", "pa_decode_workspace_size",
+                 "pa_decode_partition_tokens", "pa_last_device_error",
+                 "pa_strerror"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_binding_exposes_same_names():
+    for n in declared_functions():
+        assert hasattr(pa, n), n
+
+
+def test_strerror_names_every_status(L):
+    for code in range(0, -15, -1):
+        s = pa.pa_strerror(code)
+        assert s and "unknown" not in s, code
+    assert "unknown" in pa.pa_strerror(-999)
+
+
+# Host validation: every case returns before any CUDA call, so no GPU is needed.
+FAKE = 0x1000  # 16-byte aligned, never dereferenced on these paths
+
+
+def _decode(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, ctx=FAKE, out=FAKE, scale=0.1,
+             hq=32, hkv=8, d=128, p=16, b=2, mb=8, pages=16, dtype=0, pt=0,
+             ws=None, wsb=0)
+    a.update(kw)
+    return L.pa_decode(a["q"], a["k"], a["v"], a["bt"], a["ctx"], a["out"],
+                       ctypes.c_float(a["scale"]), a["hq"], a["hkv"], a["d"], a["p"],
+                       a["b"], a["mb"], a["pages"], a["dtype"], a["pt"], a["ws"],
+                       a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(out=None), -1), (dict(bt=None), -1),
+    (dict(hq=30, hkv=8), -2), (dict(hkv=0), -2), (dict(hq=-4), -2),
+    (dict(d=96), -3), (dict(d=256), -3),
+    (dict(p=8), -4), (dict(p=32), -4),
+    (dict(b=0), -5), (dict(mb=0), -5), (dict(pages=0), -5), (dict(b=70000), -5),
+    (dict(pages=(1 << 31) // (8 * 16)), -5),
+    (dict(dtype=2), -6),
+    (dict(q=FAKE + 8), -8), (dict(k=FAKE + 2), -8), (dict(out=FAKE + 4), -8),
+    (dict(pt=24), -9), (dict(pt=-16), -9),
+    (dict(pt=16, ws=None, wsb=0), -7),
+])
+def test_decode_rejects_bad_arguments(L, kw, code):
+    assert _decode(L, **kw) == code
+
+
+def test_workspace_size_matches_layout(L):
+    # explicit partitions: batch * heads * parts * (D + 2) floats
+    for b, hq, hkv, d, mb, pt in [(4, 64, 8, 128, 2048, 512), (3, 8, 8, 64, 5, 32),
+                                  (1, 16, 16, 128, 32, 512)]:
+        n_parts = -(-mb * 16 // pt) if pt < mb * 16 else 1
+        want = b * hq * n_parts * (d + 2) * 4 if n_parts > 1 else 0
+        assert L.pa_decode_workspace_size(b, hq, hkv, d, 16, mb, pt) == want
+        got_pt = L.pa_decode_partition_tokens(b, hq, hkv, d, 16, mb, pt)
+        assert got_pt == (pt if n_parts > 1 else 0)
+    assert L.pa_decode_workspace_size(1, 30, 8, 128, 16, 8, 0) == 0  # invalid -> 0
+
+
+def test_auto_partition_is_page_aligned_and_bounded(L):
+    for b, hq, hkv, mb in [(8, 32, 32, 256), (64, 32, 8, 512), (4, 64, 8, 2048),
+                           (1, 16, 16, 32), (1, 1, 1, 1)]:
+        pt = L.pa_decode_partition_tokens(b, hq, hkv, 128, 16, mb, 0)
+        assert pt >= 0 and pt % 16 == 0 and pt < mb * 16 + 1
+        if pt:
+            n_parts = -(-mb * 16 // pt)
+            assert L.pa_decode_workspace_size(b, hq, hkv, 128, 16, mb, 0) == \
+                b * hq * n_parts * 130 * 4
+
+
+def test_append_and_prefill_reject_bad_arguments(L):
+    P = FAKE
+    assert L.pa_append_kv(None, P, P, P, P, P, P, 1, 8, 128, 16, 2, 8, 16, 0, None) == -1
+    assert L.pa_append_kv(P, P, P, P, P, P, P, 1, 8, 100, 16, 2, 8, 16, 0, None) == -3
+    assert L.pa_append_kv(P, P, P, P, P, P, P, -1, 8, 128, 16, 2, 8, 16, 0, None) == -5
+    assert L.pa_append_kv(P + 4, P, P, P, P, P, P, 1, 8, 128, 16, 2, 8, 16, 0, None) == -8
+    assert L.pa_append_kv(P, P, P, P, P, P, P, 0, 8, 128, 16, 2, 8, 16, 0, None) == 0
+    f = ctypes.c_float(0.1)
+    assert L.pa_prefill_paged(P, P, P, P, P, 4, None, f, 32, 8, 128, 16, 2, 8, 16, 0, None) == -1
+    assert L.pa_prefill_paged(P, P, P, P, P, 4, P, f, 32, 7, 128, 16, 2, 8, 16, 0, None) == -2
+    assert L.pa_prefill_paged(P, P, P, P, P, -1, P, f, 32, 8, 128, 16, 2, 8, 16, 0, None) == -5
+    assert L.pa_prefill_paged(P, P, P, P, P, 0, P, f, 32, 8, 128, 16, 2, 8, 16, 0, None) == 0
+    assert L.pa_merge_partials(P, P, P, 2, 8, 128, 4, 0, None) == -9
+    assert L.pa_merge_partials(P, P, P, 2, 8, 80, 4, 16, None) == -3
+    assert L.pa_merge_partials(None, P, P, 2, 8, 128, 4, 16, None) == -1
+
+
+def test_product_package_does_not_reach_the_oracle():
+    """The product path never imports, links or runs anything under oracle/."""
+    pkg = os.path.dirname(pa.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "pa_oracle" not in text and "liboracle" not in text, f

@@ -14,8 +14,8 @@ Recipe (the pages publish no dataset; their workloads are LLaMA-7B-shaped,
     (layer, sequence, logical block) order, to the block tables.  Unused
     block-table entries are -1 so that a kernel that reads past a sequence's
     last block is caught by its own bounds check.
-  * Context lengths are given, or drawn uniformly (inclusive) by the same
-    generator.
+  * Context lengths are given (an int or a list), or drawn uniformly from an
+    inclusive (lo, hi) tuple by the same generator.
 """
 from __future__ import annotations
 
@@ -98,7 +98,7 @@ def _fill_normal(dst: torch.Tensor, gen: torch.Generator, mul: float = 1.0,
 
 
 def draw_ctx_lens(batch: int, ctx, gen: torch.Generator) -> torch.Tensor:
-    if isinstance(ctx, (tuple, list)) and len(ctx) == 2:
+    if isinstance(ctx, tuple):  # (lo, hi): uniform, inclusive
         lo, hi = ctx
         return torch.randint(lo, hi + 1, (batch,), generator=gen,
                              dtype=torch.int64).to(torch.int32)

@@ -62,7 +62,9 @@ enum {
   PA_ERR_BAD_BLOCK = -11,  /* device: block-table entry outside [0, num_pages) */
   PA_ERR_BAD_CTX = -12,    /* device: context length < 0 or beyond the table */
   PA_ERR_TIMEOUT = -13,    /* device: a bounded wait for a copy ran out */
-  PA_ERR_BAD_INDEX = -14   /* device: append seq_idx / pos outside the table */
+  PA_ERR_BAD_INDEX = -14,  /* device: append seq_idx / pos outside the table */
+  PA_ERR_SCRATCH_LIMIT = -15 /* pa_decode_static_workspace: the call needs more
+                                split-K scratch than its fixed 16 MiB array */
 };
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -179,6 +181,39 @@ int pa_prefill_paged(const void *q, const void *k_cache, const void *v_cache,
                      int n_kv_heads, int head_dim, int page_size, int batch,
                      int max_blocks_per_seq, int num_pages, pa_dtype dtype,
                      pa_stream_t stream);
+
+/*
+ * pa_decode_static_workspace -- pa_decode for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this entry point: it is a convenience of
+ * this library.  Some callers cannot call cudaMalloc: code embedded in a host
+ * framework that owns every device allocation (a private allocation would
+ * bypass its allocator and its accounting), code on a latency-critical path
+ * where cudaMalloc/cudaFree may synchronise the whole device, or code that
+ * only speaks this C ABI and has no allocator.  This entry point computes
+ * exactly what pa_decode computes, with the same arguments minus the
+ * workspace: the split-K partial states go to a 16 MiB array that lives in
+ * the library's device image (every GPU that loads the library holds it until
+ * the process exits).  It allocates nothing and frees nothing.
+ *
+ * Limit: a call whose partition plan needs more than 16 MiB of scratch
+ * (pa_decode_workspace_size() > 16 MiB; e.g. batch * n_q_heads * n_parts *
+ * (head_dim + 2) * 4 bytes above that) returns PA_ERR_SCRATCH_LIMIT and
+ * launches nothing.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array and leaves its contents behind;
+ * nothing in it needs to start at zero.  Calls that overlap on the GPU (two
+ * streams, or two host threads, with split-K plans) race on the array: the
+ * caller must order them.
+ */
+int pa_decode_static_workspace(const void *q, const void *k_cache,
+                               const void *v_cache, const int32_t *block_table,
+                               const int32_t *ctx_lens, float *out, float scale,
+                               int n_q_heads, int n_kv_heads, int head_dim,
+                               int page_size, int batch, int max_blocks_per_seq,
+                               int num_pages, pa_dtype dtype,
+                               int partition_tokens, pa_stream_t stream);
 
 /*
  * pa_last_device_error -- synchronise `stream`, then return and clear the

@@ -19,6 +19,7 @@ import os
 __all__ = [
     "PAError", "BF16", "F16", "lib", "dtype_code", "pa_decode",
     "pa_decode_partition_tokens", "pa_decode_workspace_size",
+    "pa_decode_static_workspace",
     "pa_merge_partials", "pa_append_kv", "pa_prefill_paged",
     "pa_last_device_error", "pa_strerror", "decode", "prefill", "append_kv",
 ]
@@ -63,6 +64,8 @@ def lib():
         L.pa_append_kv.restype = I
         L.pa_prefill_paged.argtypes = [P, P, P, P, P, I, P, F] + [I] * 8 + [P]
         L.pa_prefill_paged.restype = I
+        L.pa_decode_static_workspace.argtypes = [P, P, P, P, P, P, F] + [I] * 9 + [P]
+        L.pa_decode_static_workspace.restype = I
         L.pa_last_device_error.argtypes = [P]
         L.pa_last_device_error.restype = I
         _lib = L
@@ -120,6 +123,19 @@ def pa_decode(q, k_cache, v_cache, block_table, ctx_lens, out, scale, n_q_heads,
                          max_blocks_per_seq, num_pages, dtype, partition_tokens,
                          _ptr(workspace), workspace_bytes, _stream(stream))
     return _check(rc, "pa_decode")
+
+
+def pa_decode_static_workspace(q, k_cache, v_cache, block_table, ctx_lens, out,
+                               scale, n_q_heads, n_kv_heads, head_dim, page_size,
+                               batch, max_blocks_per_seq, num_pages, dtype,
+                               partition_tokens=0, stream=None) -> int:
+    """pa_decode with its split-K scratch in the library's fixed 16 MiB
+    device array: for callers that cannot allocate device memory."""
+    rc = lib().pa_decode_static_workspace(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens),
+        _ptr(out), float(scale), n_q_heads, n_kv_heads, head_dim, page_size, batch,
+        max_blocks_per_seq, num_pages, dtype, partition_tokens, _stream(stream))
+    return _check(rc, "pa_decode_static_workspace")
 
 
 def pa_decode_partition_tokens(batch, n_q_heads, n_kv_heads, head_dim, page_size,

@@ -207,6 +207,8 @@ const char *pa_strerror(int status) {
     case PA_ERR_BAD_CTX: return "PA_ERR_BAD_CTX: context length outside [0, max_blocks*page_size]";
     case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded wait for a copy ran out";
     case PA_ERR_BAD_INDEX: return "PA_ERR_BAD_INDEX: append seq_idx/pos outside the table";
+    case PA_ERR_SCRATCH_LIMIT:
+      return "PA_ERR_SCRATCH_LIMIT: needs more split-K scratch than the 16 MiB static array";
     default: return "unknown pa status";
   }
 }

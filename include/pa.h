@@ -99,7 +99,8 @@ const char *pa_strerror(int status);
  *                many tokens and merged
  *   workspace    device, >= pa_decode_workspace_size(...) bytes, 16-byte
  *                aligned; may be NULL when that size is 0.  Holds the
- *                partial states; contents on entry do not matter.
+ *                partial states; contents on entry do not matter.  Two calls
+ *                that overlap on the GPU must not share a workspace.
  * q, k_cache, v_cache, out and workspace must be 16-byte aligned.
  */
 int pa_decode(const void *q, const void *k_cache, const void *v_cache,
@@ -117,14 +118,16 @@ int pa_decode_partition_tokens(int batch, int n_q_heads, int n_kv_heads,
                                int max_blocks_per_seq, int partition_tokens);
 
 /* Workspace bytes pa_decode needs for the same arguments (0 when it runs in a
- * single pass).  Layout: float [batch][n_q_heads][n_parts][head_dim + 2],
- * each row (O_p[0..head_dim-1], m_p, l_p) with m_p in natural-log units. */
+ * single pass).  Layout: float [batch][n_q_heads][n_parts][head_dim + 4],
+ * each row (O_p[0..head_dim-1], m_p, l_p, 2 unused) with m_p in natural-log
+ * units. */
 size_t pa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
                                 int head_dim, int page_size,
                                 int max_blocks_per_seq, int partition_tokens);
 
 /*
- * pa_merge_partials -- the exact merge of partition states on its own.
+ * pa_merge_partials -- the exact merge of partition states on its own (the
+ * same arithmetic pa_decode runs in its last partition's CTA).
  *
  * For row (b, h) with n = ceil(ctx_lens[b] / partition_tokens) valid parts
  * p < n (parts at p >= n are not read):
@@ -132,7 +135,8 @@ size_t pa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
  * (the exponent law e^(a+b) = e^a e^b of ch. 19 19.6.2, applied to two
  * summarised chunks).  A part with l_p = 0 contributes nothing; a row with
  * none writes zeros.
- *   partials  device float [batch][n_q_heads][n_parts][head_dim + 2]
+ *   partials  device float [batch][n_q_heads][n_parts][head_dim + 4], rows
+ *             (O_p[0..head_dim-1], m_p, l_p, 2 unused), 16-byte aligned
  *   out       device float [batch][n_q_heads][head_dim]
  */
 int pa_merge_partials(const float *partials, const int32_t *ctx_lens,
@@ -197,8 +201,8 @@ int pa_prefill_paged(const void *q, const void *k_cache, const void *v_cache,
  * the process exits).  It allocates nothing and frees nothing.
  *
  * Limit: a call whose partition plan needs more than 16 MiB of scratch
- * (pa_decode_workspace_size() > 16 MiB; e.g. batch * n_q_heads * n_parts *
- * (head_dim + 2) * 4 bytes above that) returns PA_ERR_SCRATCH_LIMIT and
+ * (pa_decode_workspace_size() > 16 MiB; about batch * n_q_heads * n_parts *
+ * (head_dim + 4) * 4 bytes above that) returns PA_ERR_SCRATCH_LIMIT and
  * launches nothing.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

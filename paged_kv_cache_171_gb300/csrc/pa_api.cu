@@ -154,27 +154,33 @@ int sm_count() {
 }
 
 // Partition plan of pa_decode: pages per partition (0 = single pass) and the
-// partition count.  Automatic mode cuts sequences so that the grid holds a
-// few waves of resident CTAs even when batch * heads is small, and so that
-// one long sequence cannot make a tail of its own.
+// partition count.  Automatic mode, with R = resident CTAs (2 per SM) and
+// I = batch * kv heads * head tiles (CTAs of a single pass):
+//   I <  3R/4: cut sequences into about R / I equal partitions, so that one
+//              wave of CTAs keeps enough copies in flight;
+//   I <  R   : a single pass (one wave, no merge);
+//   I >= R   : cut into 4 partitions of >= 32 pages, so that one long
+//              sequence of a ragged batch cannot make a tail of its own.
 int decode_plan(int batch, int n_q_heads, int n_kv_heads, int max_blocks,
                 int partition_tokens, int *part_pages, int *n_parts) {
   if (partition_tokens < 0 || partition_tokens % kPageSize) return PA_ERR_PARTITION;
   int pp = partition_tokens / kPageSize;
   if (pp == 0) {
     const int sms = sm_count() > 0 ? sm_count() : 148;
-    const int64_t resident = static_cast<int64_t>(sms) * 2;  // CTAs per SM
+    const int64_t resident = static_cast<int64_t>(sms) * 2;
     const int64_t items = static_cast<int64_t>(batch) * n_kv_heads *
                           ((n_q_heads / n_kv_heads) / group_tile(n_q_heads / n_kv_heads));
-    // aim for ~8 partition-sized CTAs per resident slot if every sequence were
-    // full-length, but never cut below 16 pages (256 tokens)
-    int64_t target = (items * max_blocks + resident * 8 - 1) / (resident * 8);
-    if (target < 16) target = 16;
-    if (target >= max_blocks) {
+    if (items * 4 < resident * 3) {
+      const int64_t want = resident / items > 1 ? resident / items : 1;
+      int64_t per = (max_blocks + want - 1) / want;
+      if (per < 16) per = 16;
+      pp = static_cast<int>(per);
+    } else if (items < resident) {
       pp = 0;
     } else {
-      const int64_t np = (max_blocks + target - 1) / target;
-      pp = static_cast<int>((max_blocks + np - 1) / np);  // equal-sized parts
+      int64_t per = (max_blocks + 3) / 4;
+      if (per < 32) per = 32;
+      pp = static_cast<int>(per);
     }
   }
   if (pp >= max_blocks) pp = 0;
@@ -236,7 +242,7 @@ size_t pa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
                   partition_tokens, &pp, &np))
     return 0;
   if (np <= 1) return 0;
-  return static_cast<size_t>(batch) * n_q_heads * np * (head_dim + 2) * sizeof(float);
+  return decode_partials_bytes(batch, n_q_heads, np, head_dim);
 }
 
 int pa_decode(const void *q, const void *k_cache, const void *v_cache,
@@ -257,8 +263,7 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
                    partition_tokens, &pp, &np);
   if (rc) return rc;
   if (np > 1) {
-    const size_t need =
-        static_cast<size_t>(batch) * n_q_heads * np * (head_dim + 2) * sizeof(float);
+    const size_t need = decode_partials_bytes(batch, n_q_heads, np, head_dim);
     if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PA_ERR_ALIGN;
   }

@@ -1,4 +1,4 @@
-// pa_decode.cu -- decode-step paged GQA attention for sm_103a (CUDA cores).
+// pa_decode.cu -- decode-step paged GQA attention for sm_103a.
 //
 // Computes, per sequence b and query head h, o = softmax(q K^T * scale) V
 // over the sequence's cached tokens (ch. 19 "推理系统与性能工程", 19.4.1),
@@ -14,20 +14,30 @@
 // swizzle) that complete on one mbarrier per stage, and issues the load for
 // page i+S as soon as page i has been consumed.  No warp waits for another
 // until the partition's end, where the warps' (m, l, O) states are merged in
-// shared memory with the exponent law of 19.6.2.
+// shared memory with the exponent law of 19.6.2.  A sequence cut into several
+// partitions leaves one partial state per partition; merge_kernel combines
+// them exactly (same law).
 //
-// Score phase: lane = (token, half of head_dim).  The swizzled tile lets the
-// 16 lanes of a half-warp read 16 different K rows without bank conflicts
-// while all of them read the same q element (a broadcast).
-// Value phase: lane = head_dim / 32 output dims; every lane reads the same V
-// row.  Both phases use packed fp32x2 FMAs; K/V elements are unpacked from
-// bf16/fp16 once per page and reused by all GT heads.
+// Per-page math, chosen by the group tile:
+//  * GT = 1 (MHA): CUDA cores.  Score phase lane = (token, half of head_dim):
+//    the swizzled tile lets 16 lanes read 16 different K rows without bank
+//    conflicts while sharing each q element; value phase lane = head_dim/32
+//    output dims.  Packed fp32x2 FMAs.
+//  * GT >= 2 (GQA): the group's q K^T (GT heads x 16 keys x head_dim) and
+//    P V are dense contractions, so they run on the tensor cores as warp-level
+//    mma.sync m16n8k16 with the heads as rows (padded to 16).  K and V
+//    fragments come straight from the swizzled page tiles with ldmatrix; q
+//    stays in registers.  On CUDA cores every lane would re-read all GT q rows
+//    from shared memory for every page, which made that path shared-memory
+//    bound at GT = 8; this way shared-memory traffic is the K/V bytes alone.
+//    P enters P V as two 16-bit terms (head + remainder) so the weights keep
+//    ~16 significant bits.
 //
-// Scores are kept in log2 units (q is pre-multiplied by scale * log2 e), so
-// e^(s - m) is one ex2.  The running max is only moved when a score exceeds it
-// by more than kRescaleSlack (a warp vote decides); between moves the
-// weights e^(s - m) stay <= 2^kRescaleSlack.  The rescale is exact whatever
-// reference max is used, because O and l share it (19.6.2's argument).
+// Scores are kept in log2 units (scale * log2 e folded in), so e^(s - m) is
+// one ex2.  The running max is only moved when a score exceeds it by more than
+// kRescaleSlack (a warp vote decides); between moves the weights e^(s - m)
+// stay <= 2^kRescaleSlack.  The rescale is exact whatever reference max is
+// used, because O and l share it (19.6.2's argument).
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -44,7 +54,7 @@ struct DecodeParams {
   const int32_t *block_table;
   const int32_t *ctx_lens;
   float *out;
-  float *ws;
+  float *ws;  // partial states [B][Hq][n_parts][D + 4]
   int *status;
   float qscale;  // scale * log2(e)
   int n_q_heads, n_kv_heads, group, batch, max_blocks, num_pages;
@@ -52,17 +62,20 @@ struct DecodeParams {
 };
 
 // Shared-memory plan of one CTA.
-template <int D, int GT, int NW, int S>
+template <int D, int GT, int NW, int S, bool MMA>
 struct DecodeSmem {
   static constexpr int kBoxBytes = 16 * 128;  // one TMA box: 16 rows x 64 elems
   static constexpr int kBoxes = D / 64;
   static constexpr int kPageBytes = kBoxes * kBoxBytes;  // K (or V) of one page
   static constexpr int kStageBytes = 2 * kPageBytes;     // K tile then V tile
   static constexpr int kStages = NW * S;
-  static constexpr int kQStride = D + 8;  // floats per q row; 2nd half +4
+  static constexpr int kQStride = D + 8;  // CUDA-core path: floats per q row
+  // q: fp32 rows (CUDA cores) or a swizzled 16-row bf16/fp16 tile (MMA)
+  static constexpr int kQBytes = MMA ? 16 * D * 2 : GT * kQStride * 4;
+  static constexpr int kPBytes = MMA ? 0 : NW * GT * 16 * 4;
   static constexpr int kQOff = kStages * kStageBytes;
-  static constexpr int kPOff = kQOff + GT * kQStride * 4;
-  static constexpr int kBarOff = kPOff + NW * GT * 16 * 4;
+  static constexpr int kPOff = kQOff + kQBytes;
+  static constexpr int kBarOff = kPOff + kPBytes;
   static constexpr int kBytes = kBarOff + kStages * 8;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-B alignment
   static constexpr int kMergeFloats = NW * GT * (D + 2);
@@ -70,150 +83,97 @@ struct DecodeSmem {
   static_assert(kStageBytes % 1024 == 0, "swizzled boxes need 1024-B alignment");
 };
 
-template <int D, int GT, bool BF16, int NW, int S>
-__global__ void __launch_bounds__(NW * 32)
-    decode_kernel(const __grid_constant__ CUtensorMap kmap,
-                  const __grid_constant__ CUtensorMap vmap,
-                  const DecodeParams p) {
-  using L = DecodeSmem<D, GT, NW, S>;
-  constexpr int DPL = D / 32;   // output dims per lane
-  constexpr int HALF = D / 2;   // dims per half-warp in the score phase
-  constexpr int CPH = HALF / 8; // 16-byte chunks per half row
+// Byte offset of 16-byte chunk c (0 .. D/8-1) of row r in a tile stored as
+// 64-column boxes of `box_rows` rows with the TMA 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int r, int c, int box_rows) {
+  return (c >> 3) * (box_rows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  float *q_s = reinterpret_cast<float *>(smem + L::kQOff);
+// One warp's ring of S page stages and the page ids that feed it.  Chunk i
+// of the warp is logical block first + NW * i of the sequence.
+template <int D, int NW, int S>
+struct PageRing {
+  static constexpr int kBoxBytes = 16 * 128;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kPageBytes = kBoxes * kBoxBytes;
+  static constexpr int kStageBytes = 2 * kPageBytes;
+  uint32_t stage0, bar0;
+  const int32_t *bt_row;
+  int *status;
+  int first, n_i, num_pages, y_page, y_head;
+  int ids_cur, ids_nxt;
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int part = blockIdx.x;
-  const int n_sub = p.group / GT;
-  const int g = blockIdx.y / n_sub;
-  const int h0 = g * p.group + (blockIdx.y % n_sub) * GT;
-  const int b = blockIdx.z;
-
-  int T = p.ctx_lens[b];
-  const int maxT = p.max_blocks * 16;
-  if (T < 0 || T > maxT) {
-    if (tid == 0) record_error(p.status, PA_ERR_BAD_CTX);
-    T = T < 0 ? 0 : maxT;
-  }
-  const int n_pages = (T + 15) >> 4;
-  int pg0 = 0, pg1 = n_pages;
-  if (p.part_pages > 0) {
-    pg0 = part * p.part_pages;
-    pg1 = min(n_pages, pg0 + p.part_pages);
-  }
-  if (pg0 >= pg1) {
-    // Nothing to read.  A single pass owes zeros; with partitions the merge
-    // kernel never reads a partition past the sequence's end.
-    if (p.n_parts == 1)
-      for (int i = tid; i < GT * D; i += NW * 32)
-        p.out[(static_cast<size_t>(b) * p.n_q_heads + h0) * D + i] = 0.f;
-    return;
-  }
-
-  if (tid == 0) {
-    for (int s = 0; s < L::kStages; ++s) mbar_init(sbase + L::kBarOff + 8 * s, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  // ---- this warp's pages: logical blocks first, first+NW, first+2NW, ...
-  const int first = pg0 + warp;
-  const int n_i = first < pg1 ? (pg1 - first + NW - 1) / NW : 0;
-  const int32_t *bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-  auto fetch_id = [&](int i) -> int {
+  __device__ int fetch_id(int i) {
     if (i >= n_i) return 0;
     int id = __ldg(bt_row + first + NW * i);
-    if (static_cast<unsigned>(id) >= static_cast<unsigned>(p.num_pages)) {
-      record_error(p.status, PA_ERR_BAD_BLOCK);
+    if (static_cast<unsigned>(id) >= static_cast<unsigned>(num_pages)) {
+      record_error(status, PA_ERR_BAD_BLOCK);
       id = 0;  // read a page that exists; the result is flagged as invalid
     }
     return id;
-  };
+  }
   // Lane j holds the page of chunk 32k + j; the next 32 are fetched early.
-  int ids_cur = fetch_id(lane);
-  int ids_nxt = fetch_id(32 + lane);
-  const uint32_t stage0 = sbase + warp * S * L::kStageBytes;
-  const uint32_t bar0 = sbase + L::kBarOff + warp * S * 8;
-  const int rows_per_page = p.n_kv_heads * 16;
-
-  auto issue = [&](int i) {  // called by the whole warp, i = 0, 1, 2, ...
+  __device__ void start(int lane) {
+    ids_cur = fetch_id(lane);
+    ids_nxt = fetch_id(32 + lane);
+  }
+  __device__ uint32_t stage(int i) const { return stage0 + (i % S) * kStageBytes; }
+  __device__ uint32_t bar(int i) const { return bar0 + 8 * (i % S); }
+  __device__ uint32_t parity(int i) const { return (i / S) & 1; }
+  // Called by the whole warp with i = 0, 1, 2, ... in order.
+  __device__ void issue(int i, int lane, const CUtensorMap *kmap, const CUtensorMap *vmap) {
     if ((i & 31) == 0 && i > 0) {
       ids_cur = ids_nxt;
       ids_nxt = fetch_id(i + 32 + lane);
     }
     const int id = __shfl_sync(kFull, ids_cur, i & 31);
     if (lane == 0) {
-      const int s = i % S;
-      const uint32_t st = stage0 + s * L::kStageBytes, bar = bar0 + 8 * s;
+      const uint32_t st = stage(i), b = bar(i);
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, L::kStageBytes);
-      const int y = id * rows_per_page + g * 16;
+      mbar_arrive_expect_tx(b, kStageBytes);
+      const int y = id * y_page + y_head;
 #pragma unroll
-      for (int bx = 0; bx < L::kBoxes; ++bx) {
-        tma_load_2d(st + bx * L::kBoxBytes, &kmap, bx * 64, y, bar);
-        tma_load_2d(st + L::kPageBytes + bx * L::kBoxBytes, &vmap, bx * 64, y, bar);
-      }
-    }
-  };
-
-  for (int i = 0; i < S && i < n_i; ++i) issue(i);
-
-  // ---- q of the head tile -> shared memory as fp32 * scale * log2(e)
-  {
-    const uint16_t *qg = p.q + (static_cast<size_t>(b) * p.n_q_heads + h0) * D;
-    for (int e = tid * 8; e < GT * D; e += NW * 32 * 8) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(qg + e);
-      const int h = e / D, d = e % D;
-      float *dst = q_s + h * L::kQStride + d + (d >= HALF ? 4 : 0);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = unpack2<BF16>(w[k]);
-        dst[2 * k] = f.x * p.qscale;
-        dst[2 * k + 1] = f.y * p.qscale;
+      for (int bx = 0; bx < kBoxes; ++bx) {
+        tma_load_2d(st + bx * kBoxBytes, kmap, bx * 64, y, b);
+        tma_load_2d(st + kPageBytes + bx * kBoxBytes, vmap, bx * 64, y, b);
       }
     }
   }
-  __syncthreads();
-
-  float m[GT], lsum[GT];
-  float2 O2[GT][DPL / 2];
-#pragma unroll
-  for (int h = 0; h < GT; ++h) {
-    m[h] = -INFINITY;
-    lsum[h] = 0.f;
-#pragma unroll
-    for (int k = 0; k < DPL / 2; ++k) O2[h][k] = make_float2(0.f, 0.f);
+  // Warp-uniform wait for chunk i; on a timeout, records it, lets the other
+  // copies in flight land, and returns false.
+  __device__ bool wait(int i, int lane) {
+    if (__all_sync(kFull, mbar_wait(bar(i), parity(i)))) return true;
+    if (lane == 0) record_error(status, PA_ERR_TIMEOUT);
+    for (int j = i + 1; j < n_i && j < i + S; ++j) mbar_wait(bar(j), parity(j));
+    return false;
   }
-  float *p_s = reinterpret_cast<float *>(smem + L::kPOff) + warp * GT * 16;
+};
+
+// ---------------------------------------------------------------------------
+// CUDA-core page loop (GT = 1, or any GT): per-warp (m, l, O) in registers.
+template <int D, int GT, bool BF16, int NW, int S, class Ring>
+__device__ __forceinline__ void pages_cuda_core(Ring &ring, const CUtensorMap *kmap,
+                                                const CUtensorMap *vmap,
+                                                const float *q_s, float *p_s, int T,
+                                                int lane, float (&m)[GT],
+                                                float (&lsum)[GT],
+                                                float2 (&O2)[GT][D / 64]) {
+  constexpr int DPL = D / 32;
+  constexpr int HALF = D / 2;
+  constexpr int CPH = HALF / 8;
+  constexpr int QS = D + 8;
   const int tok = lane & 15, hf = lane >> 4;
-  // score phase: this lane's K row inside a stage
-  const uint32_t k_off = (D == 128 ? hf * L::kBoxBytes : 0) + tok * 128;
-  // value phase: this lane's dims inside a V row, before the swizzle
-  const uint32_t v_off = L::kPageBytes +
-                         (D == 128 ? (lane >> 4) * L::kBoxBytes + ((lane & 1) << 3)
+  const uint32_t k_off = (D == 128 ? hf * Ring::kBoxBytes : 0) + tok * 128;
+  const uint32_t v_off = Ring::kPageBytes +
+                         (D == 128 ? (lane >> 4) * Ring::kBoxBytes + ((lane & 1) << 3)
                                    : ((lane & 3) << 2));
   const int v_chunk = (D == 128) ? ((lane & 15) >> 1) : (lane >> 2);
 
-  for (int i = 0; i < n_i; ++i) {
-    const int s = i % S;
-    const uint32_t st = stage0 + s * L::kStageBytes;
-    // The verdict is made warp-uniform so that no lane leaves the loop alone.
-    if (!__all_sync(kFull, mbar_wait(bar0 + 8 * s, (i / S) & 1))) {
-      if (lane == 0) record_error(p.status, PA_ERR_TIMEOUT);
-      // Let the other copies this warp has in flight land before leaving.
-      for (int j = i + 1; j < n_i && j < i + S; ++j)
-        mbar_wait(bar0 + 8 * (j % S), (j / S) & 1);
-      break;
-    }
-    const int t0 = (first + NW * i) * 16;
-    const int valid = min(16, T - t0);
+  for (int i = 0; i < ring.n_i; ++i) {
+    if (!ring.wait(i, lane)) break;
+    const uint32_t st = ring.stage(i);
+    const int valid = min(16, T - (ring.first + NW * i) * 16);
 
-    // -- scores s_h(tok) = <q_h, k_tok>, already * scale * log2 e
     float sc[GT];
     {
       float2 acc[GT];
@@ -228,7 +188,7 @@ __global__ void __launch_bounds__(NW * 32)
         const float2 k45 = unpack2<BF16>(kv.z), k67 = unpack2<BF16>(kv.w);
 #pragma unroll
         for (int h = 0; h < GT; ++h) {
-          const float *qh = q_s + h * L::kQStride + hf * (HALF + 4) + j * 8;
+          const float *qh = q_s + h * QS + hf * (HALF + 4) + j * 8;
           const float4 qa = *reinterpret_cast<const float4 *>(qh);
           const float4 qb = *reinterpret_cast<const float4 *>(qh + 4);
           acc[h] = __ffma2_rn(make_float2(qa.x, qa.y), k01, acc[h]);
@@ -245,7 +205,6 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
 
-    // -- online softmax: move the reference max only when needed
     bool need = false;
 #pragma unroll
     for (int h = 0; h < GT; ++h) need |= sc[h] > m[h] + kRescaleSlack;
@@ -274,9 +233,8 @@ __global__ void __launch_bounds__(NW * 32)
     }
     __syncwarp();
 
-    // -- O_h += sum_t p_h(t) v_t over the page's valid tokens
     const uint32_t vrow = st + v_off;
-    auto pv = [&](int t, const float (&pw)[GT]) {
+    auto pv = [&](int t, const float(&pw)[GT]) {
       const uint32_t addr = vrow + t * 128 + ((v_chunk ^ (t & 7)) << 4);
       if constexpr (D == 128) {
         const uint2 vv = lds64(addr);
@@ -311,6 +269,7 @@ __global__ void __launch_bounds__(NW * 32)
         }
       }
     } else {
+      // V rows past the sequence end are never read.
       for (int t = 0; t < valid; ++t) {
         float pw[GT];
 #pragma unroll
@@ -319,12 +278,10 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
     __syncwarp();
-    if (i + S < n_i) issue(i + S);
+    if (i + S < ring.n_i) ring.issue(i + S, lane, kmap, vmap);
   }
-
-  // ---- l: each token was counted by one lane of each half-warp
 #pragma unroll
-  for (int h = 0; h < GT; ++h) {
+  for (int h = 0; h < GT; ++h) {  // each token was counted once per half-warp
     float v = lsum[h];
     v += __shfl_xor_sync(kFull, v, 8);
     v += __shfl_xor_sync(kFull, v, 4);
@@ -332,27 +289,251 @@ __global__ void __launch_bounds__(NW * 32)
     v += __shfl_xor_sync(kFull, v, 1);
     lsum[h] = v;
   }
+}
 
-  // ---- merge the NW warp states (the stages are free once all warps are here)
+// ---------------------------------------------------------------------------
+// Tensor-core page loop (GT >= 2).  Row r = lane / 4 of the accumulators is
+// query head r of the tile (rows >= GT are padding); this lane holds keys
+// k0, k0+1, k0+8, k0+9 of the page (k0 = 2 * (lane % 4)) and output dims
+// 8n + k0, 8n + k0 + 1.
+template <int D, int GT, bool BF16, int NW, int S, class Ring>
+__device__ __forceinline__ void pages_mma(Ring &ring, const CUtensorMap *kmap,
+                                          const CUtensorMap *vmap, uint32_t qs,
+                                          float qscale, int T, int lane, float &m_r,
+                                          float &l_r, float (&o)[D / 8][4]) {
+  constexpr int KS = D / 16;
+  constexpr int NT = D / 8;
+  uint32_t qa[KS][4];
+  {
+    const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk)
+      ldsm_x4(qs + swz(r, 2 * kk + (lane >> 4), 16), qa[kk][0], qa[kk][1], qa[kk][2],
+              qa[kk][3]);
+  }
+  const bool real = (lane >> 2) < GT;
+  const int k0 = 2 * (lane & 3);
+  const int rk = ((lane >> 4) << 3) + (lane & 7);       // K ldmatrix row
+  const int rv = (lane & 7) + (((lane >> 3) & 1) << 3);  // V ldmatrix row
+
+  for (int i = 0; i < ring.n_i; ++i) {
+    if (!ring.wait(i, lane)) break;
+    const uint32_t st = ring.stage(i);
+    const int valid = min(16, T - (ring.first + NW * i) * 16);
+    if (valid < 16) {
+      // V rows past the sequence end may hold non-finite junk, and 0 * inf is
+      // NaN inside the MMA: clear them (the next TMA overwrites the stage).
+      const int n = (16 - valid) * (D / 8);
+      for (int e = lane; e < n; e += 32) {
+        const int r = valid + e / (D / 8), c = e % (D / 8);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                         st + Ring::kPageBytes + swz(r, c, 16)),
+                     "r"(0));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+
+    float sacc[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(st + swz(rk, 2 * kk + ((lane >> 3) & 1), 16), b0, b1, b2, b3);
+      mma16816<BF16>(sacc[0], qa[kk], b0, b1);
+      mma16816<BF16>(sacc[1], qa[kk], b2, b3);
+    }
+    float s[4] = {sacc[0][0] * qscale, sacc[0][1] * qscale, sacc[1][0] * qscale,
+                  sacc[1][1] * qscale};
+    const int keys[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[j] = (real && keys[j] < valid) ? s[j] : -INFINITY;
+    const float tmax = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+    if (__any_sync(kFull, tmax > m_r + kRescaleSlack)) {
+      float mt = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
+      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+      const float mn = fmaxf(m_r, mt);
+      const float c = mn == -INFINITY ? 1.f : ex2(m_r - mn);
+      m_r = mn;
+      l_r *= c;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        o[n][0] *= c;
+        o[n][1] *= c;
+      }
+    }
+    float p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) p[j] = real ? ex2(s[j] - m_r) : 0.f;
+    l_r += (p[0] + p[1]) + (p[2] + p[3]);
+    const uint32_t h01 = pack2<BF16>(p[0], p[1]), h89 = pack2<BF16>(p[2], p[3]);
+    const float2 r01 = unpack2<BF16>(h01), r89 = unpack2<BF16>(h89);
+    const uint32_t pa[4] = {h01, 0u, h89, 0u};
+    const uint32_t pb[4] = {pack2<BF16>(p[0] - r01.x, p[1] - r01.y), 0u,
+                            pack2<BF16>(p[2] - r89.x, p[3] - r89.y), 0u};
+#pragma unroll
+    for (int nn = 0; nn < NT / 2; ++nn) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(st + Ring::kPageBytes + swz(rv, 2 * nn + (lane >> 4), 16), b0, b1, b2, b3);
+      mma16816<BF16>(o[2 * nn], pa, b0, b1);
+      mma16816<BF16>(o[2 * nn + 1], pa, b2, b3);
+      mma16816<BF16>(o[2 * nn], pb, b0, b1);
+      mma16816<BF16>(o[2 * nn + 1], pb, b2, b3);
+    }
+    __syncwarp();
+    if (i + S < ring.n_i) ring.issue(i + S, lane, kmap, vmap);
+  }
+  l_r += __shfl_xor_sync(kFull, l_r, 1);
+  l_r += __shfl_xor_sync(kFull, l_r, 2);
+}
+
+// ---------------------------------------------------------------------------
+template <int D, int GT, bool BF16, int NW, int S, bool MMA>
+__global__ void __launch_bounds__(NW * 32)
+    decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap,
+                  const DecodeParams p) {
+  using L = DecodeSmem<D, GT, NW, S, MMA>;
+  using Ring = PageRing<D, NW, S>;
+  constexpr int HALF = D / 2;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int part = blockIdx.x;
+  const int n_sub = p.group / GT;
+  const int g = blockIdx.y / n_sub;
+  const int h0 = g * p.group + (blockIdx.y % n_sub) * GT;
+  const int b = blockIdx.z;
+
+  int T = p.ctx_lens[b];
+  const int maxT = p.max_blocks * 16;
+  if (T < 0 || T > maxT) {
+    if (tid == 0) record_error(p.status, PA_ERR_BAD_CTX);
+    T = T < 0 ? 0 : maxT;
+  }
+  const int n_pages = (T + 15) >> 4;
+  int pg0 = 0, pg1 = n_pages;
+  if (p.part_pages > 0) {
+    pg0 = part * p.part_pages;
+    pg1 = min(n_pages, pg0 + p.part_pages);
+  }
+  if (pg0 >= pg1) {
+    // Nothing to read.  An empty sequence owes zeros (partition 0 writes
+    // them); the merge never reads a partition past a sequence's end.
+    if (part == 0)
+      for (int i = tid; i < GT * D; i += NW * 32)
+        p.out[(static_cast<size_t>(b) * p.n_q_heads + h0) * D + i] = 0.f;
+    return;
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < L::kStages; ++s) mbar_init(sbase + L::kBarOff + 8 * s, 1);
+    fence_mbar_init();
+  }
   __syncthreads();
+
+  Ring ring;
+  ring.stage0 = sbase + warp * S * L::kStageBytes;
+  ring.bar0 = sbase + L::kBarOff + warp * S * 8;
+  ring.bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+  ring.status = p.status;
+  ring.first = pg0 + warp;
+  ring.n_i = ring.first < pg1 ? (pg1 - ring.first + NW - 1) / NW : 0;
+  ring.num_pages = p.num_pages;
+  ring.y_page = p.n_kv_heads * 16;
+  ring.y_head = g * 16;
+  ring.start(lane);
+  for (int i = 0; i < S && i < ring.n_i; ++i) ring.issue(i, lane, &kmap, &vmap);
+
+  // ---- q of the head tile -> shared memory (overlaps the first copies)
+  const uint16_t *qg = p.q + (static_cast<size_t>(b) * p.n_q_heads + h0) * D;
+  if constexpr (MMA) {
+    const uint32_t qs = sbase + L::kQOff;
+    for (int e = tid; e < 16 * (D / 8); e += NW * 32) {
+      const int r = e / (D / 8), c = e % (D / 8);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < GT) v = *reinterpret_cast<const uint4 *>(qg + r * D + c * 8);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(qs + swz(r, c, 16)),
+                   "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+    }
+  } else {
+    float *q_s = reinterpret_cast<float *>(smem + L::kQOff);
+    for (int e = tid * 8; e < GT * D; e += NW * 32 * 8) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(qg + e);
+      const int h = e / D, d = e % D;
+      float *dst = q_s + h * L::kQStride + d + (d >= HALF ? 4 : 0);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = unpack2<BF16>(w[k]);
+        dst[2 * k] = f.x * p.qscale;
+        dst[2 * k + 1] = f.y * p.qscale;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- stream the pages, then leave this warp's state in shared memory
   float *mer_m = reinterpret_cast<float *>(smem);
   float *mer_l = mer_m + NW * GT;
   float *mer_o = mer_l + NW * GT;
-  if (lane == 0) {
+  if constexpr (MMA) {
+    float m_r = -INFINITY, l_r = 0.f;
+    float o[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    pages_mma<D, GT, BF16, NW, S>(ring, &kmap, &vmap, sbase + L::kQOff, p.qscale, T, lane,
+                                  m_r, l_r, o);
+    __syncthreads();  // every warp is done with its stages
+    const int r = lane >> 2;
+    if (r < GT) {
+      if ((lane & 3) == 0) {
+        mer_m[warp * GT + r] = m_r;
+        mer_l[warp * GT + r] = l_r;
+      }
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n)
+        *reinterpret_cast<float2 *>(mer_o + (warp * GT + r) * D + n * 8 + 2 * (lane & 3)) =
+            make_float2(o[n][0], o[n][1]);
+    }
+  } else {
+    float m[GT], lsum[GT];
+    float2 O2[GT][D / 64];
 #pragma unroll
     for (int h = 0; h < GT; ++h) {
-      mer_m[warp * GT + h] = m[h];
-      mer_l[warp * GT + h] = lsum[h];
+      m[h] = -INFINITY;
+      lsum[h] = 0.f;
+#pragma unroll
+      for (int k = 0; k < D / 64; ++k) O2[h][k] = make_float2(0.f, 0.f);
     }
+    float *p_s = reinterpret_cast<float *>(smem + L::kPOff) + warp * GT * 16;
+    pages_cuda_core<D, GT, BF16, NW, S>(ring, &kmap, &vmap,
+                                        reinterpret_cast<const float *>(smem + L::kQOff),
+                                        p_s, T, lane, m, lsum, O2);
+    __syncthreads();  // every warp is done with its stages
+    if (lane == 0) {
+#pragma unroll
+      for (int h = 0; h < GT; ++h) {
+        mer_m[warp * GT + h] = m[h];
+        mer_l[warp * GT + h] = lsum[h];
+      }
+    }
+    constexpr int DPL = D / 32;
+#pragma unroll
+    for (int h = 0; h < GT; ++h)
+#pragma unroll
+      for (int k = 0; k < DPL / 2; ++k)
+        *reinterpret_cast<float2 *>(mer_o + (warp * GT + h) * D + lane * DPL + 2 * k) =
+            O2[h][k];
   }
-#pragma unroll
-  for (int h = 0; h < GT; ++h)
-#pragma unroll
-    for (int k = 0; k < DPL / 2; ++k)
-      *reinterpret_cast<float2 *>(mer_o + (warp * GT + h) * D + lane * DPL + 2 * k) =
-          O2[h][k];
   __syncthreads();
 
+  // ---- merge the NW warp states: final output, or this partition's state
   for (int e = tid; e < GT * D; e += NW * 32) {
     const int h = e / D, d = e % D;
     float M = -INFINITY;
@@ -371,7 +552,7 @@ __global__ void __launch_bounds__(NW * 32)
     if (p.n_parts == 1) {
       p.out[row * D + d] = lt > 0.f ? o / lt : 0.f;
     } else {
-      float *dst = p.ws + (row * p.n_parts + part) * (D + 2);
+      float *dst = p.ws + (row * p.n_parts + part) * (D + 4);
       dst[d] = o;
       if (d == 0) {
         dst[D] = M * kLn2;  // natural-log units
@@ -381,45 +562,88 @@ __global__ void __launch_bounds__(NW * 32)
   }
 }
 
-// ---- exact merge of partition states: one CTA of head_dim threads per row
+// ---------------------------------------------------------------------------
+// Exact merge of partition states (the exponent law: M = max m_p,
+// l = sum e^(m_p - M) l_p, o = sum e^(m_p - M) O_p / l), one CTA of 8 warps
+// per (sequence, head).  Warp w folds parts w, w + 8, ... into a running state
+// (its lanes own head_dim / 32 dims each), then the 8 states are folded the
+// same way through shared memory.
 template <int D>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(256)
     merge_kernel(const float *__restrict__ parts, const int32_t *__restrict__ ctx,
-                 float *__restrict__ out, int *status, int n_q_heads,
-                 int n_parts, int part_tokens) {
-  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+                 float *__restrict__ out, int *status, int n_q_heads, int n_parts,
+                 int part_tokens) {
+  constexpr int W = D + 4, DPL = D / 32;
+  __shared__ float sm[8], sl[8];
+  __shared__ __align__(16) float so[8][D];
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   long T = ctx[b];
   if (T < 0) {
-    if (d == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
+    if (threadIdx.x == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
     T = 0;
   }
   int n_valid = static_cast<int>((T + part_tokens - 1) / part_tokens);
   if (n_valid > n_parts) {
-    if (d == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
+    if (threadIdx.x == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
     n_valid = n_parts;
   }
   const size_t row = static_cast<size_t>(b) * n_q_heads + h;
-  const float *src = parts + row * n_parts * (D + 2);
-  float M = -INFINITY;
-  for (int q = 0; q < n_valid; ++q) {
-    const float *sp = src + q * (D + 2);
-    if (sp[D + 1] > 0.f) M = fmaxf(M, sp[D]);
-  }
-  float lt = 0.f, o = 0.f;
-  if (M != -INFINITY) {
-    for (int q = 0; q < n_valid; ++q) {
-      const float *sp = src + q * (D + 2);
-      const float l = sp[D + 1];
-      if (!(l > 0.f)) continue;
-      const float f = ex2((sp[D] - M) * kLog2e);
-      lt += f * l;
-      o += f * sp[d];
+  const float *base = parts + row * static_cast<size_t>(n_parts) * W;
+  float m = -INFINITY, l = 0.f, o[DPL];
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) o[k] = 0.f;
+#pragma unroll 2
+  for (int q = warp; q < n_valid; q += 8) {
+    const float *sp = base + static_cast<size_t>(q) * W;
+    const float2 ml = __ldg(reinterpret_cast<const float2 *>(sp + D));
+    float v[DPL];
+    if constexpr (DPL == 4) {
+      const float4 t = __ldg(reinterpret_cast<const float4 *>(sp) + lane);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      const float2 t = __ldg(reinterpret_cast<const float2 *>(sp) + lane);
+      v[0] = t.x; v[1] = t.y;
     }
+    if (!(ml.y > 0.f)) continue;
+    const float mn = fmaxf(m, ml.x);
+    const float c_old = m == -INFINITY ? 0.f : ex2((m - mn) * kLog2e);
+    const float c_new = ex2((ml.x - mn) * kLog2e);
+    l = l * c_old + ml.y * c_new;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) o[k] = o[k] * c_old + v[k] * c_new;
+    m = mn;
   }
-  out[row * D + d] = lt > 0.f ? o / lt : 0.f;
+  if (lane == 0) {
+    sm[warp] = m;
+    sl[warp] = l;
+  }
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) so[warp][lane * DPL + k] = o[k];
+  __syncthreads();
+  if (warp == 0) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) M = fmaxf(M, sm[w]);
+    float lt = 0.f, acc[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float f = sm[w] == -INFINITY ? 0.f : ex2((sm[w] - M) * kLog2e);
+        lt += f * sl[w];
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) acc[k] += f * so[w][lane * DPL + k];
+      }
+    }
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) out[row * D + lane * DPL + k] = acc[k] * inv;
+  }
 }
 
-// Stages per warp: keep about 24 KiB of K/V per warp in flight.
+// Stages per warp: about 24 KiB of K/V per warp in the ring.
 template <int D>
 constexpr int stages_per_warp() { return D == 128 ? 3 : 6; }
 constexpr int kDecodeWarps = 4;
@@ -427,8 +651,9 @@ constexpr int kDecodeWarps = 4;
 template <int D, int GT, bool BF16>
 int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   constexpr int NW = kDecodeWarps, S = stages_per_warp<D>();
-  using L = DecodeSmem<D, GT, NW, S>;
-  auto kern = decode_kernel<D, GT, BF16, NW, S>;
+  constexpr bool MMA = GT >= 2;
+  using L = DecodeSmem<D, GT, NW, S, MMA>;
+  auto kern = decode_kernel<D, GT, BF16, NW, S, MMA>;
   static uint64_t attr_set = 0;  // one bit per device ordinal
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return PA_ERR_CUDA;
@@ -463,9 +688,9 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   if (a.n_parts > 1) {
     const dim3 mgrid(a.n_q_heads, a.batch);
-    merge_kernel<D><<<mgrid, D, 0, stream>>>(a.workspace, a.ctx_lens, a.out,
-                                             a.status, a.n_q_heads, a.n_parts,
-                                             a.part_pages * 16);
+    merge_kernel<D><<<mgrid, 256, 0, stream>>>(a.workspace, a.ctx_lens, a.out,
+                                               a.status, a.n_q_heads, a.n_parts,
+                                               a.part_pages * 16);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
@@ -496,13 +721,11 @@ int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,
                  int n_parts, int partition_tokens, cudaStream_t stream) {
   const dim3 grid(n_q_heads, batch);
   if (head_dim == 128)
-    merge_kernel<128><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                                n_q_heads, n_parts,
-                                                partition_tokens);
+    merge_kernel<128><<<grid, 256, 0, stream>>>(partials, ctx_lens, out, status,
+                                                n_q_heads, n_parts, partition_tokens);
   else
-    merge_kernel<64><<<grid, 64, 0, stream>>>(partials, ctx_lens, out, status,
-                                              n_q_heads, n_parts,
-                                              partition_tokens);
+    merge_kernel<64><<<grid, 256, 0, stream>>>(partials, ctx_lens, out, status,
+                                               n_q_heads, n_parts, partition_tokens);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -32,6 +32,12 @@ struct DecodeLaunch {
 
 int launch_decode(const DecodeLaunch &a, cudaStream_t stream);
 
+// Workspace of a split pa_decode: float partial states [B][Hq][n_parts][D + 4]
+// (O_p, m_p, l_p, two unused floats: rows stay 16-byte aligned).
+inline size_t decode_partials_bytes(int batch, int n_q_heads, int n_parts, int head_dim) {
+  return static_cast<size_t>(batch) * n_q_heads * n_parts * (head_dim + 4) * sizeof(float);
+}
+
 int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,
                  int *status, int batch, int n_q_heads, int head_dim,
                  int n_parts, int partition_tokens, cudaStream_t stream);

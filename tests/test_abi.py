@@ -82,12 +82,16 @@ def test_decode_rejects_bad_arguments(L, kw, code):
     assert _decode(L, **kw) == code
 
 
+def _ws_bytes(b, hq, hkv, d, n_parts):
+    """batch * heads * parts * (D + 4) floats."""
+    return b * hq * n_parts * (d + 4) * 4
+
+
 def test_workspace_size_matches_layout(L):
-    # explicit partitions: batch * heads * parts * (D + 2) floats
     for b, hq, hkv, d, mb, pt in [(4, 64, 8, 128, 2048, 512), (3, 8, 8, 64, 5, 32),
-                                  (1, 16, 16, 128, 32, 512)]:
+                                  (1, 16, 16, 128, 32, 512), (2, 12, 2, 64, 9, 16)]:
         n_parts = -(-mb * 16 // pt) if pt < mb * 16 else 1
-        want = b * hq * n_parts * (d + 2) * 4 if n_parts > 1 else 0
+        want = _ws_bytes(b, hq, hkv, d, n_parts) if n_parts > 1 else 0
         assert L.pa_decode_workspace_size(b, hq, hkv, d, 16, mb, pt) == want
         got_pt = L.pa_decode_partition_tokens(b, hq, hkv, d, 16, mb, pt)
         assert got_pt == (pt if n_parts > 1 else 0)
@@ -102,7 +106,7 @@ def test_auto_partition_is_page_aligned_and_bounded(L):
         if pt:
             n_parts = -(-mb * 16 // pt)
             assert L.pa_decode_workspace_size(b, hq, hkv, 128, 16, mb, 0) == \
-                b * hq * n_parts * 130 * 4
+                _ws_bytes(b, hq, hkv, 128, n_parts)
 
 
 def test_append_and_prefill_reject_bad_arguments(L):

@@ -98,7 +98,9 @@ def test_merge_partials_matches_oracle_merge():
     parts = oracle.partials(cpu.q[0], cpu.k_cache, cpu.v_cache, cpu.block_table[0],
                             cpu.ctx_lens, cpu.scale, cpu.dtype_code, part, n_parts)
     ref = oracle.merge(parts)
-    dev_parts = torch.tensor(parts, dtype=torch.float32)
+    # the library's rows are (O, m, l, 2 unused floats): 16-byte aligned
+    dev_parts = torch.zeros(parts.shape[:-1] + (128 + 4,), dtype=torch.float32)
+    dev_parts[..., :130] = torch.tensor(parts, dtype=torch.float32)
     for b, T in enumerate(lens):
         nv = -(-T // part)
         dev_parts[b, :, nv:] = float("nan")  # must never be read

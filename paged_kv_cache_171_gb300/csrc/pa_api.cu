@@ -162,7 +162,8 @@ int sm_count() {
 //   I >= R   : cut into 4 partitions of >= 32 pages, so that one long
 //              sequence of a ragged batch cannot make a tail of its own.
 int decode_plan(int batch, int n_q_heads, int n_kv_heads, int max_blocks,
-                int partition_tokens, int *part_pages, int *n_parts) {
+                int partition_tokens, int *part_pages, int *n_parts,
+                int *warp_parts = nullptr) {
   if (partition_tokens < 0 || partition_tokens % kPageSize) return PA_ERR_PARTITION;
   int pp = partition_tokens / kPageSize;
   if (pp == 0) {
@@ -186,6 +187,21 @@ int decode_plan(int batch, int n_q_heads, int n_kv_heads, int max_blocks,
   if (pp >= max_blocks) pp = 0;
   *part_pages = pp;
   *n_parts = pp ? (max_blocks + pp - 1) / pp : 1;
+  // Small partitions: let each warp own whole partitions (no cross-warp merge
+  // inside the CTA, prefetch across its partition boundaries), with enough
+  // partitions per warp that the grid is about one wave of resident CTAs.
+  int wp = 0;
+  if (pp > 0 && pp <= 32 && *n_parts >= kDecodeWarps) {
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    const int64_t resident = static_cast<int64_t>(sms) * 2;
+    const int64_t items = static_cast<int64_t>(batch) * n_kv_heads *
+                          ((n_q_heads / n_kv_heads) / group_tile(n_q_heads / n_kv_heads));
+    const int64_t warps = resident * kDecodeWarps;
+    int64_t w = (items * *n_parts + warps - 1) / warps;
+    const int64_t wmax = (*n_parts + kDecodeWarps - 1) / kDecodeWarps;
+    wp = static_cast<int>(w < 1 ? 1 : (w > wmax ? wmax : w));
+  }
+  if (warp_parts) *warp_parts = wp;
   return PA_OK;
 }
 
@@ -258,9 +274,9 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
   if (rc) return rc;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_ALIGN;
-  int pp = 0, np = 1;
+  int pp = 0, np = 1, wp = 0;
   rc = decode_plan(batch, n_q_heads, n_kv_heads, max_blocks_per_seq,
-                   partition_tokens, &pp, &np);
+                   partition_tokens, &pp, &np, &wp);
   if (rc) return rc;
   if (np > 1) {
     const size_t need = decode_partials_bytes(batch, n_q_heads, np, head_dim);
@@ -287,6 +303,7 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
   a.bf16 = dtype == PA_BF16;
   a.part_pages = pp;
   a.n_parts = np;
+  a.warp_parts = wp;
   return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

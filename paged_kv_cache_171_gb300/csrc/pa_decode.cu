@@ -59,6 +59,7 @@ struct DecodeParams {
   float qscale;  // scale * log2(e)
   int n_q_heads, n_kv_heads, group, batch, max_blocks, num_pages;
   int part_pages, n_parts;
+  int warp_parts;  // > 0: each warp owns this many whole partitions
 };
 
 // Shared-memory plan of one CTA.
@@ -90,7 +91,8 @@ __device__ __forceinline__ uint32_t swz(int r, int c, int box_rows) {
 }
 
 // One warp's ring of S page stages and the page ids that feed it.  Chunk i
-// of the warp is logical block first + NW * i of the sequence.
+// of the warp is logical block first + stride * i of the sequence (stride NW
+// when the CTA's warps share a partition, 1 when a warp owns whole ones).
 template <int D, int NW, int S>
 struct PageRing {
   static constexpr int kBoxBytes = 16 * 128;
@@ -100,12 +102,12 @@ struct PageRing {
   uint32_t stage0, bar0;
   const int32_t *bt_row;
   int *status;
-  int first, n_i, num_pages, y_page, y_head;
+  int first, stride, n_i, num_pages, y_page, y_head;
   int ids_cur, ids_nxt;
 
   __device__ int fetch_id(int i) {
     if (i >= n_i) return 0;
-    int id = __ldg(bt_row + first + NW * i);
+    int id = __ldg(bt_row + first + stride * i);
     if (static_cast<unsigned>(id) >= static_cast<unsigned>(num_pages)) {
       record_error(status, PA_ERR_BAD_BLOCK);
       id = 0;  // read a page that exists; the result is flagged as invalid
@@ -117,6 +119,7 @@ struct PageRing {
     ids_cur = fetch_id(lane);
     ids_nxt = fetch_id(32 + lane);
   }
+  __device__ int page(int i) const { return first + stride * i; }
   __device__ uint32_t stage(int i) const { return stage0 + (i % S) * kStageBytes; }
   __device__ uint32_t bar(int i) const { return bar0 + 8 * (i % S); }
   __device__ uint32_t parity(int i) const { return (i / S) & 1; }
@@ -151,8 +154,10 @@ struct PageRing {
 
 // ---------------------------------------------------------------------------
 // CUDA-core page loop (GT = 1, or any GT): per-warp (m, l, O) in registers.
+// Chunks [i_begin, i_end) of the warp's ring; false if a wait ran out.
 template <int D, int GT, bool BF16, int NW, int S, class Ring>
-__device__ __forceinline__ void pages_cuda_core(Ring &ring, const CUtensorMap *kmap,
+__device__ __forceinline__ bool pages_cuda_core(Ring &ring, int i_begin, int i_end,
+                                                const CUtensorMap *kmap,
                                                 const CUtensorMap *vmap,
                                                 const float *q_s, float *p_s, int T,
                                                 int lane, float (&m)[GT],
@@ -169,10 +174,11 @@ __device__ __forceinline__ void pages_cuda_core(Ring &ring, const CUtensorMap *k
                                    : ((lane & 3) << 2));
   const int v_chunk = (D == 128) ? ((lane & 15) >> 1) : (lane >> 2);
 
-  for (int i = 0; i < ring.n_i; ++i) {
-    if (!ring.wait(i, lane)) break;
+  bool ok = true;
+  for (int i = i_begin; i < i_end; ++i) {
+    if (!ring.wait(i, lane)) { ok = false; break; }
     const uint32_t st = ring.stage(i);
-    const int valid = min(16, T - (ring.first + NW * i) * 16);
+    const int valid = min(16, T - ring.page(i) * 16);
 
     float sc[GT];
     {
@@ -289,6 +295,7 @@ __device__ __forceinline__ void pages_cuda_core(Ring &ring, const CUtensorMap *k
     v += __shfl_xor_sync(kFull, v, 1);
     lsum[h] = v;
   }
+  return ok;
 }
 
 // ---------------------------------------------------------------------------
@@ -297,7 +304,8 @@ __device__ __forceinline__ void pages_cuda_core(Ring &ring, const CUtensorMap *k
 // k0, k0+1, k0+8, k0+9 of the page (k0 = 2 * (lane % 4)) and output dims
 // 8n + k0, 8n + k0 + 1.
 template <int D, int GT, bool BF16, int NW, int S, class Ring>
-__device__ __forceinline__ void pages_mma(Ring &ring, const CUtensorMap *kmap,
+__device__ __forceinline__ bool pages_mma(Ring &ring, int i_begin, int i_end,
+                                          const CUtensorMap *kmap,
                                           const CUtensorMap *vmap, uint32_t qs,
                                           float qscale, int T, int lane, float &m_r,
                                           float &l_r, float (&o)[D / 8][4]) {
@@ -316,10 +324,11 @@ __device__ __forceinline__ void pages_mma(Ring &ring, const CUtensorMap *kmap,
   const int rk = ((lane >> 4) << 3) + (lane & 7);       // K ldmatrix row
   const int rv = (lane & 7) + (((lane >> 3) & 1) << 3);  // V ldmatrix row
 
-  for (int i = 0; i < ring.n_i; ++i) {
-    if (!ring.wait(i, lane)) break;
+  bool ok = true;
+  for (int i = i_begin; i < i_end; ++i) {
+    if (!ring.wait(i, lane)) { ok = false; break; }
     const uint32_t st = ring.stage(i);
-    const int valid = min(16, T - (ring.first + NW * i) * 16);
+    const int valid = min(16, T - ring.page(i) * 16);
     if (valid < 16) {
       // V rows past the sequence end may hold non-finite junk, and 0 * inf is
       // NaN inside the MMA: clear them (the next TMA overwrites the stage).
@@ -386,6 +395,7 @@ __device__ __forceinline__ void pages_mma(Ring &ring, const CUtensorMap *kmap,
   }
   l_r += __shfl_xor_sync(kFull, l_r, 1);
   l_r += __shfl_xor_sync(kFull, l_r, 2);
+  return ok;
 }
 
 // ---------------------------------------------------------------------------
@@ -404,11 +414,11 @@ __global__ void __launch_bounds__(NW * 32)
   const uint32_t sbase = smem_u32(smem);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int part = blockIdx.x;
   const int n_sub = p.group / GT;
   const int g = blockIdx.y / n_sub;
   const int h0 = g * p.group + (blockIdx.y % n_sub) * GT;
   const int b = blockIdx.z;
+  const int ppw = p.warp_parts;  // > 0: every warp owns ppw whole partitions
 
   int T = p.ctx_lens[b];
   const int maxT = p.max_blocks * 16;
@@ -417,18 +427,24 @@ __global__ void __launch_bounds__(NW * 32)
     T = T < 0 ? 0 : maxT;
   }
   const int n_pages = (T + 15) >> 4;
-  int pg0 = 0, pg1 = n_pages;
-  if (p.part_pages > 0) {
-    pg0 = part * p.part_pages;
-    pg1 = min(n_pages, pg0 + p.part_pages);
-  }
-  if (pg0 >= pg1) {
-    // Nothing to read.  An empty sequence owes zeros (partition 0 writes
-    // them); the merge never reads a partition past a sequence's end.
-    if (part == 0)
-      for (int i = tid; i < GT * D; i += NW * 32)
-        p.out[(static_cast<size_t>(b) * p.n_q_heads + h0) * D + i] = 0.f;
-    return;
+  int pg0 = 0, pg1 = n_pages;  // this CTA's pages
+  if (ppw > 0) {
+    pg0 = blockIdx.x * NW * ppw * p.part_pages;
+    pg1 = min(n_pages, pg0 + NW * ppw * p.part_pages);
+    if (pg0 >= pg1) return;  // the merge writes zeros for an empty sequence
+  } else {
+    if (p.part_pages > 0) {
+      pg0 = blockIdx.x * p.part_pages;
+      pg1 = min(n_pages, pg0 + p.part_pages);
+    }
+    if (pg0 >= pg1) {
+      // Nothing to read.  An empty sequence owes zeros (partition 0 writes
+      // them); the merge never reads a partition past a sequence's end.
+      if (blockIdx.x == 0)
+        for (int i = tid; i < GT * D; i += NW * 32)
+          p.out[(static_cast<size_t>(b) * p.n_q_heads + h0) * D + i] = 0.f;
+      return;
+    }
   }
 
   if (tid == 0) {
@@ -442,8 +458,15 @@ __global__ void __launch_bounds__(NW * 32)
   ring.bar0 = sbase + L::kBarOff + warp * S * 8;
   ring.bt_row = p.block_table + static_cast<size_t>(b) * p.max_blocks;
   ring.status = p.status;
-  ring.first = pg0 + warp;
-  ring.n_i = ring.first < pg1 ? (pg1 - ring.first + NW - 1) / NW : 0;
+  if (ppw > 0) {  // warp w: partitions blockIdx.x * NW * ppw + w * ppw + [0, ppw)
+    ring.first = pg0 + warp * ppw * p.part_pages;
+    ring.stride = 1;
+    ring.n_i = max(0, min(pg1, ring.first + ppw * p.part_pages) - ring.first);
+  } else {        // warp w: pages pg0 + w, pg0 + w + NW, ...
+    ring.first = pg0 + warp;
+    ring.stride = NW;
+    ring.n_i = ring.first < pg1 ? (pg1 - ring.first + NW - 1) / NW : 0;
+  }
   ring.num_pages = p.num_pages;
   ring.y_page = p.n_kv_heads * 16;
   ring.y_head = g * 16;
@@ -478,19 +501,42 @@ __global__ void __launch_bounds__(NW * 32)
   }
   __syncthreads();
 
-  // ---- stream the pages, then leave this warp's state in shared memory
+  const size_t row0 = static_cast<size_t>(b) * p.n_q_heads + h0;
   float *mer_m = reinterpret_cast<float *>(smem);
   float *mer_l = mer_m + NW * GT;
   float *mer_o = mer_l + NW * GT;
   if constexpr (MMA) {
-    float m_r = -INFINITY, l_r = 0.f;
-    float o[D / 8][4];
+    const int r = lane >> 2, k0 = 2 * (lane & 3);
+    float m_r, l_r, o[D / 8][4];
+    auto reset = [&] {
+      m_r = -INFINITY;
+      l_r = 0.f;
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    pages_mma<D, GT, BF16, NW, S>(ring, &kmap, &vmap, sbase + L::kQOff, p.qscale, T, lane,
-                                  m_r, l_r, o);
+      for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    };
+    if (ppw > 0) {
+      // ---- each partition's state goes straight from registers to memory
+      for (int k = 0; k < ppw && k * p.part_pages < ring.n_i; ++k) {
+        reset();
+        const bool ok = pages_mma<D, GT, BF16, NW, S>(
+            ring, k * p.part_pages, min(ring.n_i, (k + 1) * p.part_pages), &kmap, &vmap,
+            sbase + L::kQOff, p.qscale, T, lane, m_r, l_r, o);
+        const int part = (ring.first / p.part_pages) + k;
+        if (r < GT) {
+          float *dst = p.ws + ((row0 + r) * p.n_parts + part) * (D + 4);
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n)
+            *reinterpret_cast<float2 *>(dst + n * 8 + k0) = make_float2(o[n][0], o[n][1]);
+          if ((lane & 3) == 0) *reinterpret_cast<float2 *>(dst + D) = make_float2(m_r * kLn2, l_r);
+        }
+        if (!ok) break;
+      }
+      return;
+    }
+    reset();
+    pages_mma<D, GT, BF16, NW, S>(ring, 0, ring.n_i, &kmap, &vmap, sbase + L::kQOff,
+                                  p.qscale, T, lane, m_r, l_r, o);
     __syncthreads();  // every warp is done with its stages
-    const int r = lane >> 2;
     if (r < GT) {
       if ((lane & 3) == 0) {
         mer_m[warp * GT + r] = m_r;
@@ -498,23 +544,46 @@ __global__ void __launch_bounds__(NW * 32)
       }
 #pragma unroll
       for (int n = 0; n < D / 8; ++n)
-        *reinterpret_cast<float2 *>(mer_o + (warp * GT + r) * D + n * 8 + 2 * (lane & 3)) =
+        *reinterpret_cast<float2 *>(mer_o + (warp * GT + r) * D + n * 8 + k0) =
             make_float2(o[n][0], o[n][1]);
     }
   } else {
+    constexpr int DPL = D / 32;
     float m[GT], lsum[GT];
     float2 O2[GT][D / 64];
+    auto reset = [&] {
 #pragma unroll
-    for (int h = 0; h < GT; ++h) {
-      m[h] = -INFINITY;
-      lsum[h] = 0.f;
+      for (int h = 0; h < GT; ++h) {
+        m[h] = -INFINITY;
+        lsum[h] = 0.f;
 #pragma unroll
-      for (int k = 0; k < D / 64; ++k) O2[h][k] = make_float2(0.f, 0.f);
-    }
+        for (int k = 0; k < D / 64; ++k) O2[h][k] = make_float2(0.f, 0.f);
+      }
+    };
     float *p_s = reinterpret_cast<float *>(smem + L::kPOff) + warp * GT * 16;
-    pages_cuda_core<D, GT, BF16, NW, S>(ring, &kmap, &vmap,
-                                        reinterpret_cast<const float *>(smem + L::kQOff),
-                                        p_s, T, lane, m, lsum, O2);
+    const float *q_s = reinterpret_cast<const float *>(smem + L::kQOff);
+    if (ppw > 0) {
+      for (int k = 0; k < ppw && k * p.part_pages < ring.n_i; ++k) {
+        reset();
+        const bool ok = pages_cuda_core<D, GT, BF16, NW, S>(
+            ring, k * p.part_pages, min(ring.n_i, (k + 1) * p.part_pages), &kmap, &vmap, q_s,
+            p_s, T, lane, m, lsum, O2);
+        const int part = (ring.first / p.part_pages) + k;
+#pragma unroll
+        for (int h = 0; h < GT; ++h) {
+          float *dst = p.ws + ((row0 + h) * p.n_parts + part) * (D + 4);
+#pragma unroll
+          for (int kk = 0; kk < DPL / 2; ++kk)
+            *reinterpret_cast<float2 *>(dst + lane * DPL + 2 * kk) = O2[h][kk];
+          if (lane == 0) *reinterpret_cast<float2 *>(dst + D) = make_float2(m[h] * kLn2, lsum[h]);
+        }
+        if (!ok) break;
+      }
+      return;
+    }
+    reset();
+    pages_cuda_core<D, GT, BF16, NW, S>(ring, 0, ring.n_i, &kmap, &vmap, q_s, p_s, T, lane, m,
+                                        lsum, O2);
     __syncthreads();  // every warp is done with its stages
     if (lane == 0) {
 #pragma unroll
@@ -523,7 +592,6 @@ __global__ void __launch_bounds__(NW * 32)
         mer_l[warp * GT + h] = lsum[h];
       }
     }
-    constexpr int DPL = D / 32;
 #pragma unroll
     for (int h = 0; h < GT; ++h)
 #pragma unroll
@@ -534,6 +602,7 @@ __global__ void __launch_bounds__(NW * 32)
   __syncthreads();
 
   // ---- merge the NW warp states: final output, or this partition's state
+  const int part = blockIdx.x;
   for (int e = tid; e < GT * D; e += NW * 32) {
     const int h = e / D, d = e % D;
     float M = -INFINITY;
@@ -548,7 +617,7 @@ __global__ void __launch_bounds__(NW * 32)
         o += f * mer_o[(w * GT + h) * D + d];
       }
     }
-    const size_t row = static_cast<size_t>(b) * p.n_q_heads + h0 + h;
+    const size_t row = row0 + h;
     if (p.n_parts == 1) {
       p.out[row * D + d] = lt > 0.f ? o / lt : 0.f;
     } else {
@@ -564,89 +633,97 @@ __global__ void __launch_bounds__(NW * 32)
 
 // ---------------------------------------------------------------------------
 // Exact merge of partition states (the exponent law: M = max m_p,
-// l = sum e^(m_p - M) l_p, o = sum e^(m_p - M) O_p / l), one CTA of 8 warps
-// per (sequence, head).  Warp w folds parts w, w + 8, ... into a running state
-// (its lanes own head_dim / 32 dims each), then the 8 states are folded the
-// same way through shared memory.
+// l = sum e^(m_p - M) l_p, o = sum e^(m_p - M) O_p / l), one CTA of 128
+// threads per (sequence, head).  Every load of a pass is independent of the
+// others, so a row costs a few memory round trips however many partitions:
+// pass 1 reduces M and l over the partitions' (m, l) pairs; pass 2 gives each
+// thread a float4 of head_dim and every SL-th partition; the SL slices are
+// summed through shared memory.
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(128)
     merge_kernel(const float *__restrict__ parts, const int32_t *__restrict__ ctx,
                  float *__restrict__ out, int *status, int n_q_heads, int n_parts,
                  int part_tokens) {
-  constexpr int W = D + 4, DPL = D / 32;
-  __shared__ float sm[8], sl[8];
-  __shared__ __align__(16) float so[8][D];
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int W = D + 4, Q = D / 4, SL = 128 / Q;
+  __shared__ float red[4];
+  __shared__ __align__(16) float sacc[SL][D];
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   long T = ctx[b];
   if (T < 0) {
-    if (threadIdx.x == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
+    if (tid == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
     T = 0;
   }
   int n_valid = static_cast<int>((T + part_tokens - 1) / part_tokens);
   if (n_valid > n_parts) {
-    if (threadIdx.x == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
+    if (tid == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
     n_valid = n_parts;
   }
   const size_t row = static_cast<size_t>(b) * n_q_heads + h;
   const float *base = parts + row * static_cast<size_t>(n_parts) * W;
-  float m = -INFINITY, l = 0.f, o[DPL];
+
+  auto block_reduce = [&](float v, bool is_max) {
 #pragma unroll
-  for (int k = 0; k < DPL; ++k) o[k] = 0.f;
-#pragma unroll 2
-  for (int q = warp; q < n_valid; q += 8) {
-    const float *sp = base + static_cast<size_t>(q) * W;
-    const float2 ml = __ldg(reinterpret_cast<const float2 *>(sp + D));
-    float v[DPL];
-    if constexpr (DPL == 4) {
-      const float4 t = __ldg(reinterpret_cast<const float4 *>(sp) + lane);
-      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-    } else {
-      const float2 t = __ldg(reinterpret_cast<const float2 *>(sp) + lane);
-      v[0] = t.x; v[1] = t.y;
+    for (int o = 16; o > 0; o >>= 1) {
+      const float u = __shfl_xor_sync(0xffffffffu, v, o);
+      v = is_max ? fmaxf(v, u) : v + u;
     }
-    if (!(ml.y > 0.f)) continue;
-    const float mn = fmaxf(m, ml.x);
-    const float c_old = m == -INFINITY ? 0.f : ex2((m - mn) * kLog2e);
-    const float c_new = ex2((ml.x - mn) * kLog2e);
-    l = l * c_old + ml.y * c_new;
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) o[k] = o[k] * c_old + v[k] * c_new;
-    m = mn;
+    __syncthreads();  // red[] is free
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    return is_max ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]))
+                  : (red[0] + red[1]) + (red[2] + red[3]);
+  };
+  float mloc = -INFINITY;
+  for (int q = tid; q < n_valid; q += 128) {
+    const float2 ml = __ldg(reinterpret_cast<const float2 *>(base + static_cast<size_t>(q) * W + D));
+    if (ml.y > 0.f) mloc = fmaxf(mloc, ml.x);
   }
-  if (lane == 0) {
-    sm[warp] = m;
-    sl[warp] = l;
+  const float M = block_reduce(mloc, true);
+  float lloc = 0.f;
+  if (M != -INFINITY)
+    for (int q = tid; q < n_valid; q += 128) {
+      const float2 ml = __ldg(reinterpret_cast<const float2 *>(base + static_cast<size_t>(q) * W + D));
+      if (ml.y > 0.f) lloc += ex2((ml.x - M) * kLog2e) * ml.y;
+    }
+  const float lt = block_reduce(lloc, false);
+
+  const int qd = tid % Q, sl = tid / Q;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+#pragma unroll 8
+    for (int q = sl; q < n_valid; q += SL) {
+      const float *sp = base + static_cast<size_t>(q) * W;
+      const float2 ml = __ldg(reinterpret_cast<const float2 *>(sp + D));
+      const float4 o4 = __ldg(reinterpret_cast<const float4 *>(sp) + qd);
+      const float f = ml.y > 0.f ? ex2((ml.x - M) * kLog2e) : 0.f;
+      acc.x += f * o4.x;
+      acc.y += f * o4.y;
+      acc.z += f * o4.z;
+      acc.w += f * o4.w;
+    }
   }
-#pragma unroll
-  for (int k = 0; k < DPL; ++k) so[warp][lane * DPL + k] = o[k];
+  *reinterpret_cast<float4 *>(&sacc[sl][4 * qd]) = acc;
   __syncthreads();
-  if (warp == 0) {
-    float M = -INFINITY;
+  if (tid < Q) {
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < 8; ++w) M = fmaxf(M, sm[w]);
-    float lt = 0.f, acc[DPL];
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        const float f = sm[w] == -INFINITY ? 0.f : ex2((sm[w] - M) * kLog2e);
-        lt += f * sl[w];
-#pragma unroll
-        for (int k = 0; k < DPL; ++k) acc[k] += f * so[w][lane * DPL + k];
-      }
+    for (int k = 0; k < SL; ++k) {
+      const float4 v = *reinterpret_cast<const float4 *>(&sacc[k][4 * tid]);
+      t.x += v.x;
+      t.y += v.y;
+      t.z += v.z;
+      t.w += v.w;
     }
     const float inv = lt > 0.f ? 1.f / lt : 0.f;
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) out[row * D + lane * DPL + k] = acc[k] * inv;
+    reinterpret_cast<float4 *>(out + row * D)[tid] =
+        make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
   }
 }
 
 // Stages per warp: about 24 KiB of K/V per warp in the ring.
 template <int D>
 constexpr int stages_per_warp() { return D == 128 ? 3 : 6; }
-constexpr int kDecodeWarps = 4;
 
 template <int D, int GT, bool BF16>
 int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
@@ -683,12 +760,15 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   p.num_pages = a.num_pages;
   p.part_pages = a.part_pages;
   p.n_parts = a.n_parts;
-  const dim3 grid(a.n_parts, a.n_kv_heads * (p.group / GT), a.batch);
+  p.warp_parts = a.warp_parts;
+  const int gx = a.warp_parts > 0 ? (a.n_parts + NW * a.warp_parts - 1) / (NW * a.warp_parts)
+                                  : a.n_parts;
+  const dim3 grid(gx, a.n_kv_heads * (p.group / GT), a.batch);
   kern<<<grid, NW * 32, L::kAlloc, stream>>>(kmap, vmap, p);
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   if (a.n_parts > 1) {
     const dim3 mgrid(a.n_q_heads, a.batch);
-    merge_kernel<D><<<mgrid, 256, 0, stream>>>(a.workspace, a.ctx_lens, a.out,
+    merge_kernel<D><<<mgrid, 128, 0, stream>>>(a.workspace, a.ctx_lens, a.out,
                                                a.status, a.n_q_heads, a.n_parts,
                                                a.part_pages * 16);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
@@ -721,10 +801,10 @@ int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,
                  int n_parts, int partition_tokens, cudaStream_t stream) {
   const dim3 grid(n_q_heads, batch);
   if (head_dim == 128)
-    merge_kernel<128><<<grid, 256, 0, stream>>>(partials, ctx_lens, out, status,
+    merge_kernel<128><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
                                                 n_q_heads, n_parts, partition_tokens);
   else
-    merge_kernel<64><<<grid, 256, 0, stream>>>(partials, ctx_lens, out, status,
+    merge_kernel<64><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
                                                n_q_heads, n_parts, partition_tokens);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

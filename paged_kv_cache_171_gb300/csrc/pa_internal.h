@@ -28,7 +28,10 @@ struct DecodeLaunch {
   bool bf16;
   int part_pages;  // pages per partition; 0 = a single pass over the sequence
   int n_parts;     // partitions per sequence (1 for a single pass)
+  int warp_parts;  // > 0: each warp owns this many whole partitions
 };
+
+constexpr int kDecodeWarps = 4;  // warps per decode CTA
 
 int launch_decode(const DecodeLaunch &a, cudaStream_t stream);
 

@@ -34,7 +34,7 @@ constexpr float kSlack = 8.0f;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRows = 128;      // M: (query, head) rows per CTA
 constexpr int kKeys = 128;      // keys per K/V tile (8 pages)
-constexpr int kConsumers = 128; // threads of the four consumer warps
+constexpr int kConsumers = 256; // eight consumer warps, two threads per row
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
 
 struct TcParams {
@@ -61,7 +61,8 @@ struct TcSmem {
   static constexpr int kPhi = kV0 + 2 * kKVBytes;
   static constexpr int kPlo = kPhi + kPBytes;
   static constexpr int kBars = kPlo + kPBytes;  // 12 mbarriers
-  static constexpr int kSlot = kBars + 12 * 8;  // TMEM address, abort flag
+  static constexpr int kXchg = kBars + 12 * 8;  // per-row halves: max, sum
+  static constexpr int kSlot = kXchg + 2 * kRows * 4;  // TMEM address, abort flag
   static constexpr int kBytes = kSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
@@ -160,8 +161,8 @@ __device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t
                                               volatile int *abort_flag, int tid, int warp,
                                               int lane);
 
-// Consumer warps 0-3 (thread r owns row r); thread 0 also issues the MMAs.
-// Warp 4 produces the K/V tiles.
+// Consumer warps 0-7 (threads r and r + 128 share row r % 128); thread 0 also
+// issues the MMAs.  Warp 8 produces the K/V tiles.
 template <int D, int GT, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -239,6 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 template <int D, int GT, bool BF16>
 __device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t tO,
                                               const TcParams &p, int b, int q0, int hbase,
@@ -247,13 +257,20 @@ __device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t
                                               int lane) {
   using L = TcSmem<D>;
   constexpr int KSQ = D / 16;
-  constexpr int NCH = D / 32;
+  constexpr int HK = kKeys / 2;  // S columns (keys) per thread
+  constexpr int HD = D / 2;      // O columns per thread
   constexpr uint32_t kIdS = tc::idesc_f16(BF16, kRows, kKeys, false, false);
   constexpr uint32_t kIdO = tc::idesc_f16(BF16, kRows, D, false, true);
   auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
-  const int r = tid, qi = r / GT, hh = r % GT;
+  // Two threads per row: warps w and w + 4 reach the same TMEM lanes; `half`
+  // picks keys [64 half, 64 half + 64) of S and columns [HD half, +HD) of O.
+  const int half = warp >> 2;
+  const int r = ((warp & 3) << 5) + lane, qi = r / GT, hh = r % GT;
   const int lim = min(ctx + q0 + qi, kmax);  // last key row r sees
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const int lim_all = ctx + q0;              // every row sees keys <= this
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t x_mine = sb + L::kXchg + (half * kRows + r) * 4;
+  const uint32_t x_peer = sb + L::kXchg + ((half ^ 1) * kRows + r) * 4;
   int issued_s = 0, issued_o = 0;  // thread 0's MMA groups, for a drain on error
 
   auto issue_s = [&](int t) {  // S_t = Q K_t^T, one thread
@@ -271,14 +288,13 @@ __device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t
   auto issue_pv = [&](int t) {  // O += P_hi V_t + P_lo V_t, one thread
     const uint32_t vst = sb + L::kV0 + (t & 1) * L::kKVBytes;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const uint32_t pb = sb + (half ? L::kPlo : L::kPhi);
+    for (int ph = 0; ph < 2; ++ph) {
+      const uint32_t pb = sb + (ph ? L::kPlo : L::kPhi);
 #pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk) {
+      for (int kk = 0; kk < kKeys / 16; ++kk)
         tc::mma_f16(tO, tc::smem_desc_sw128(pb + (kk >> 2) * L::kColBlk + (kk & 3) * 32, 16, 1024),
                     tc::smem_desc_sw128(vst + kk * 2048, L::kColBlk, 1024), kIdO,
-                    (t > 0 || kk > 0 || half > 0) ? 1u : 0u);
-      }
+                    (t > 0 || kk > 0 || ph > 0) ? 1u : 0u);
     }
     tc::commit(bar(kBarO));
     tc::commit(bar(kBarVFree + (t & 1)));
@@ -292,31 +308,44 @@ __device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t
   }
   float m = -INFINITY, l = 0.f;
   for (int j = 0; j < n_tiles; ++j) {
-    // ---- S_j row -> registers; then the S buffer and K stage are free
+    const int key0 = j * kKeys;
+    const int kbase = key0 + half * HK;
+    // ---- my half of S_j's row -> registers, scaled and masked, half max
     if (!mbar_wait(bar(kBarS), j & 1)) bad = true;
     tc::fence_after_sync();
-    uint32_t sr[kKeys];
+    uint32_t sr[HK];
 #pragma unroll
-    for (int cb = 0; cb < kKeys / 32; ++cb)
-      tc::ld32(tS + lane_base + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + cb * 32));
+    for (int cb = 0; cb < HK / 32; ++cb)
+      tc::ld32(tS + lane_base + half * HK + cb * 32,
+               *reinterpret_cast<uint32_t(*)[32]>(sr + cb * 32));
     tc::wait_ld();
+    float hmax = -INFINITY;
+    if (key0 + kKeys - 1 <= lim_all) {  // no key of this tile is masked
+#pragma unroll
+      for (int c = 0; c < HK; ++c) {
+        const float v = __uint_as_float(sr[c]) * p.qscale;
+        sr[c] = __float_as_uint(v);
+        hmax = fmaxf(hmax, v);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < HK; ++c) {
+        const float v = (kbase + c <= lim) ? __uint_as_float(sr[c]) * p.qscale : -INFINITY;
+        sr[c] = __float_as_uint(v);
+        hmax = fmaxf(hmax, v);
+      }
+    }
+    st_shared_f32(x_mine, hmax);
     tc::fence_before_sync();
-    if (consumers_sync_or(bad)) { bad = true; break; }
+    if (consumers_sync_or(bad)) { bad = true; break; }  // S buffer, K stage free
     if (tid == 0 && j + 1 < n_tiles) {
       tc::fence_after_sync();
       if (mbar_wait(bar(kBarK + ((j + 1) & 1)), ((j + 1) >> 1) & 1)) issue_s(j + 1);
       else bad = true;
     }
 
-    // ---- mask, row max, lazy rescale decision
-    const int key0 = j * kKeys;
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kKeys; ++c) {
-      const float v = (key0 + c <= lim) ? __uint_as_float(sr[c]) * p.qscale : -INFINITY;
-      sr[c] = __float_as_uint(v);
-      tmax = fmaxf(tmax, v);
-    }
+    // ---- row max from both halves; lazy rescale decision (same in both)
+    const float tmax = fmaxf(hmax, ld_shared_f32(x_peer));
     const bool need = tmax > m + kSlack;
     float corr = 1.f;
     if (need) {
@@ -331,20 +360,20 @@ __device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t
       tc::fence_after_sync();
       if (__any_sync(kFull, need)) {
 #pragma unroll
-        for (int cb = 0; cb < NCH; ++cb) {
+        for (int cb = 0; cb < HD / 32; ++cb) {
           uint32_t o[32];
-          tc::ld32(tO + lane_base + cb * 32, o);
+          tc::ld32(tO + lane_base + half * HD + cb * 32, o);
           tc::wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
-          tc::st32(tO + lane_base + cb * 32, o);
+          tc::st32(tO + lane_base + half * HD + cb * 32, o);
         }
         tc::wait_st();
       }
     }
-    // ---- P = e^(s - m) as head + remainder, swizzled K-major rows
+    // ---- P = e^(s - m) as head + remainder: my 64 keys = 64-column block `half`
 #pragma unroll
-    for (int ch = 0; ch < kKeys / 8; ++ch) {
+    for (int ch = 0; ch < HK / 8; ++ch) {
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -355,7 +384,7 @@ __device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t
         const float2 hr = unpack2<BF16>(hi[k]);
         lo[k] = pack2<BF16>(p0 - hr.x, p1 - hr.y);
       }
-      const uint32_t off = (ch >> 3) * L::kColBlk + swz128(r, ch & 7);
+      const uint32_t off = half * L::kColBlk + swz128(r, ch);
       st_shared_v4(sb + L::kPhi + off, hi[0], hi[1], hi[2], hi[3]);
       st_shared_v4(sb + L::kPlo + off, lo[0], lo[1], lo[2], lo[3]);
     }
@@ -380,10 +409,11 @@ __device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t
     }
   }
 
-  // ---- O / l, one write per row
+  // ---- O / l, one write per row (each thread its HD columns)
   if (!bad && !mbar_wait(bar(kBarO), (n_tiles - 1) & 1)) bad = true;
   tc::fence_after_sync();
-  if (bad) {
+  st_shared_f32(x_mine, l);
+  if (consumers_sync_or(bad)) {
     if (tid == 0) {
       record_error(p.status, PA_ERR_TIMEOUT);
       *abort_flag = 1;
@@ -393,13 +423,15 @@ __device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t
     }
     return;
   }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float lt = l + ld_shared_f32(x_peer);
+  const float inv = lt > 0.f ? 1.f / lt : 0.f;
   float *dst = p.out +
-               ((static_cast<size_t>(b) * p.n_new + q0 + qi) * p.n_q_heads + hbase + hh) * D;
+               ((static_cast<size_t>(b) * p.n_new + q0 + qi) * p.n_q_heads + hbase + hh) * D +
+               half * HD;
 #pragma unroll
-  for (int cb = 0; cb < NCH; ++cb) {
+  for (int cb = 0; cb < HD / 32; ++cb) {
     uint32_t o[32];
-    tc::ld32(tO + lane_base + cb * 32, o);
+    tc::ld32(tO + lane_base + half * HD + cb * 32, o);
     tc::wait_ld();
     if (qi < nq) {
 #pragma unroll

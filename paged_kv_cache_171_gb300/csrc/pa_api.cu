@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(256)
                   const int32_t *__restrict__ pos, int *status, long total,
                   int n_kv_heads, int chunks, int batch, int max_blocks,
                   int num_pages) {
+  griddep_release();
+  griddep_wait();  // the rows may come from the previous kernel in the stream
   const long idx = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= total) return;
   const int c = static_cast<int>(idx % chunks);
@@ -111,12 +113,12 @@ int launch_append(const void *k_new, const void *v_new, void *k_cache,
   const long total = static_cast<long>(n_tok) * n_kv_heads * chunks;
   const int threads = 256;
   const long blocks = (total + threads - 1) / threads;
-  append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+  const cudaError_t e = launch_pdl(
+      append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
       static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
-      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), block_table,
-      seq_idx, pos, status, total, n_kv_heads, chunks, batch, max_blocks,
-      num_pages);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), block_table, seq_idx,
+      pos, status, total, n_kv_heads, chunks, batch, max_blocks, num_pages);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 namespace {

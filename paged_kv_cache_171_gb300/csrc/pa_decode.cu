@@ -414,6 +414,8 @@ __global__ void __launch_bounds__(NW * 32)
   const uint32_t sbase = smem_u32(smem);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  griddep_release();
+  griddep_wait();  // inputs may come from the previous kernel in the stream
   const int n_sub = p.group / GT;
   const int g = blockIdx.y / n_sub;
   const int h0 = g * p.group + (blockIdx.y % n_sub) * GT;
@@ -649,6 +651,8 @@ __global__ void __launch_bounds__(128)
   __shared__ __align__(16) float sacc[SL][D];
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  griddep_release();
+  griddep_wait();
   long T = ctx[b];
   if (T < 0) {
     if (tid == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
@@ -764,14 +768,14 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   const int gx = a.warp_parts > 0 ? (a.n_parts + NW * a.warp_parts - 1) / (NW * a.warp_parts)
                                   : a.n_parts;
   const dim3 grid(gx, a.n_kv_heads * (p.group / GT), a.batch);
-  kern<<<grid, NW * 32, L::kAlloc, stream>>>(kmap, vmap, p);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_pdl(kern, grid, dim3(NW * 32), L::kAlloc, stream, kmap, vmap, p) != cudaSuccess)
+    return PA_ERR_CUDA;
   if (a.n_parts > 1) {
     const dim3 mgrid(a.n_q_heads, a.batch);
-    merge_kernel<D><<<mgrid, 128, 0, stream>>>(a.workspace, a.ctx_lens, a.out,
-                                               a.status, a.n_q_heads, a.n_parts,
-                                               a.part_pages * 16);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_pdl(merge_kernel<D>, mgrid, dim3(128), 0, stream,
+                   static_cast<const float *>(a.workspace), a.ctx_lens, a.out, a.status,
+                   a.n_q_heads, a.n_parts, a.part_pages * 16) != cudaSuccess)
+      return PA_ERR_CUDA;
   }
   return PA_OK;
 }

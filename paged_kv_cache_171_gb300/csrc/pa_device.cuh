@@ -134,6 +134,17 @@ __device__ __forceinline__ float unpack1(uint16_t u) {
   }
 }
 
+// ---- programmatic dependent launch: a kernel launched with programmatic
+// stream serialisation may start while its predecessor in the stream is still
+// running; griddep_wait() blocks until that predecessor has completed and its
+// memory is visible, griddep_release() lets the successor start early.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- warp-level tensor-core fragments (ldmatrix + mma.sync m16n8k16)
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,

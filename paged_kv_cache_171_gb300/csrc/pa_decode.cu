@@ -105,15 +105,9 @@ struct PageRing {
   int first, stride, n_i, num_pages, y_page, y_head;
   int ids_cur, ids_nxt;
 
-  __device__ int fetch_id(int i) {
-    if (i >= n_i) return 0;
-    int id = __ldg(bt_row + first + stride * i);
-    if (static_cast<unsigned>(id) >= static_cast<unsigned>(num_pages)) {
-      record_error(status, PA_ERR_BAD_BLOCK);
-      id = 0;  // read a page that exists; the result is flagged as invalid
-    }
-    return id;
-  }
+  // The raw table entry; checked only when it is used, so the load's latency
+  // is hidden behind the 32 chunks that come first.
+  __device__ int fetch_id(int i) { return i < n_i ? __ldg(bt_row + first + stride * i) : 0; }
   // Lane j holds the page of chunk 32k + j; the next 32 are fetched early.
   __device__ void start(int lane) {
     ids_cur = fetch_id(lane);
@@ -129,8 +123,12 @@ struct PageRing {
       ids_cur = ids_nxt;
       ids_nxt = fetch_id(i + 32 + lane);
     }
-    const int id = __shfl_sync(kFull, ids_cur, i & 31);
+    int id = __shfl_sync(kFull, ids_cur, i & 31);
     if (lane == 0) {
+      if (static_cast<unsigned>(id) >= static_cast<unsigned>(num_pages)) {
+        record_error(status, PA_ERR_BAD_BLOCK);
+        id = 0;  // read a page that exists; the result is flagged as invalid
+      }
       const uint32_t st = stage(i), b = bar(i);
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(b, kStageBytes);

@@ -8,20 +8,32 @@
 //
 // Tile plan.  A CTA owns M = 128 rows = (query, head) pairs of one kv head's
 // GQA group (GT heads x 128/GT consecutive queries), so every K/V tile serves
-// the whole group ("吞吐与延迟的系统模型" 5).  Row r lives in TMEM lane r and is
-// owned by thread r of the four consumer warps.  K/V tiles are 128 keys =
-// 8 pages; a producer warp loads them page by page with 2-D TMA (128-byte
-// swizzle) into two K and two V stages laid out as the canonical K-major
-// (K) and MN-major (V) operand tiles.  Per tile j:
-//   S_j   = Q K_j^T            tcgen05.mma, M=128 N=128 K=head_dim, into TMEM
-//   softmax on S_j rows        thread r: its row from TMEM, mask, max, ex2
-//   P_j   -> shared memory     two 16-bit terms (head + remainder) so the
-//                              weights keep ~16 significant bits
-//   O    += P_j V_j            tcgen05.mma, M=128 N=head_dim K=128, in TMEM
-// S_{j+1} is issued as soon as S_j has been read, so it overlaps the softmax
-// of tile j; the softmax of tile j+1 overlaps P V of tile j.  The running max
-// moves only when a row's max exceeds it by more than 8 (log2 units); O in
-// TMEM is then rescaled in place by its row's thread.
+// the whole group ("吞吐与延迟的系统模型" 5).  K/V tiles are 128 keys = 8 pages,
+// loaded page by page with 2-D TMA (128-byte swizzle) into a ring of K and V
+// stages laid out as the canonical K-major (K) and MN-major (V) operand
+// tiles.  Per tile j:
+//   S_j   = Q K_j^T           tcgen05.mma, M=128 N=128 K=head_dim, A and B in
+//                             shared memory, into TMEM buffer j&1 (two
+//                             buffers: S_{j+1} is computed while tile j's
+//                             softmax runs)
+//   softmax                   row r is shared by two threads; each owns one
+//                             half of every tile's keys with its own running
+//                             (m, l) and its own accumulator O_half
+//   P_j   -> TMEM             written over the S_j columns its thread has
+//                             just read, as two 16-bit terms (head +
+//                             remainder) so the weights keep ~16 significant
+//                             bits
+//   O_A  += P_j[:, :64] V_j[:64],  O_B += P_j[:, 64:] V_j[64:]
+//                             tcgen05.mma with A in TMEM, B in shared memory
+// The halves are merged once at the end with the exponent law of 19.6.2.
+//
+// Warp roles: eight consumer warps (softmax), one load warp (TMA), one MMA
+// warp (a single issuing thread).  Every hand-off is an mbarrier: TMA
+// transaction counts, tcgen05.commit arrivals, and one arrival per consumer
+// warp when its half of P_j is in TMEM.  The running max moves only when a
+// score exceeds it by more than 8 (log2 units); the thread then rescales its
+// accumulator row in TMEM.  Every wait is bounded and gives up early once
+// another role has raised the CTA's abort flag.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_tcgen05.cuh"
@@ -32,10 +44,12 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.0f;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kRows = 128;      // M: (query, head) rows per CTA
-constexpr int kKeys = 128;      // keys per K/V tile (8 pages)
-constexpr int kConsumers = 256; // eight consumer warps, two threads per row
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kRows = 128;       // M: (query, head) rows per CTA
+constexpr int kKeys = 128;       // keys per K/V tile (8 pages)
+constexpr int kConsumers = 256;  // eight consumer warps, two threads per row
+constexpr int kLoadWarp = kConsumers / 32;
+constexpr int kMmaWarp = kLoadWarp + 1;
+constexpr int kThreads = kConsumers + 64;
 
 struct TcParams {
   const uint16_t *q;
@@ -51,25 +65,32 @@ struct TcParams {
 // stored as 64-column blocks of [rows][128 B] with the 128-byte swizzle.
 template <int D>
 struct TcSmem {
-  static constexpr int kColBlk = kRows * 128;   // one 64-column block, 128 rows
+  static constexpr int kStages = D == 128 ? 3 : 4;     // K and V ring depth
+  static constexpr int kColBlk = kRows * 128;          // one 64-column block, 128 rows
   static constexpr int kQBytes = (D / 64) * kColBlk;
   static constexpr int kKVBytes = (D / 64) * kColBlk;  // 128 keys x D
-  static constexpr int kPBytes = 2 * kColBlk;           // 128 rows x 128 keys
   static constexpr int kQ = 0;
   static constexpr int kK0 = kQ + kQBytes;
-  static constexpr int kV0 = kK0 + 2 * kKVBytes;
-  static constexpr int kPhi = kV0 + 2 * kKVBytes;
-  static constexpr int kPlo = kPhi + kPBytes;
-  static constexpr int kBars = kPlo + kPBytes;  // 12 mbarriers
-  static constexpr int kXchg = kBars + 12 * 8;  // per-row halves: max, sum
-  static constexpr int kSlot = kXchg + 2 * kRows * 4;  // TMEM address, abort flag
+  static constexpr int kV0 = kK0 + kStages * kKVBytes;
+  static constexpr int kBars = kV0 + kStages * kKVBytes;
+  static constexpr int kSlot = kBars + 24 * 8;  // TMEM address, abort flag
   static constexpr int kBytes = kSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
+  static_assert(2 * kRows * 8 <= kKVBytes, "final exchange must fit in one K stage");
 };
 
 // mbarrier indices
-enum { kBarK = 0, kBarV = 2, kBarKFree = 4, kBarVFree = 6, kBarS = 8, kBarO = 9 };
+enum {
+  kBarK = 0,        // K stage s landed (TMA transaction count), s < 4
+  kBarV = 4,        // V stage s landed
+  kBarKFree = 8,    // K stage s read by its S MMAs (commit)
+  kBarVFree = 12,   // V stage s read by both halves' P V MMAs (commit)
+  kBarS = 16,       // S_t ready in TMEM buffer t&1 (commit), per buffer
+  kBarO = 18,       // P V_t of key half h done (commit), per half
+  kBarPReady = 20,  // P_t of key half h in TMEM (one arrival per warp), per half
+  kNumBars = 22
+};
 
 __device__ __forceinline__ uint32_t swz128(int r, int c) {  // row r, 16-B chunk c < 8
   return r * 128 + (((c & 7) ^ (r & 7)) << 4);
@@ -96,79 +117,360 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// Producer warp: loads K_t and V_t (8 pages each) for t = 0 .. n_tiles-1.
-// Stage t & 1 of K (V) is refilled once the MMA that read it for tile t-2,
-// S_{t-2} (P V_{t-2}), has completed (its commit arrives on the free barrier).
-template <int D>
-__device__ __forceinline__ void produce_tiles(const CUtensorMap *kmap, const CUtensorMap *vmap,
-                                              uint32_t sb, const int32_t *bt_row,
-                                              int n_pages, int n_tiles, int num_pages,
-                                              int y_page, int y_head, int *status,
-                                              volatile int *abort_flag, int lane) {
-  using L = TcSmem<D>;
-  constexpr int kBoxes = D / 64;
-  auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
-  int issued[2] = {0, 0};  // K tiles, V tiles whose loads were issued
-  for (int t = 0; t < n_tiles; ++t) {
-    int id = 0;  // lane j < 8: page 8t + j (past the sequence: page 0, masked)
-    const int pg = 8 * t + (lane & 7);
-    if (lane < 8 && pg < n_pages) {
-      id = __ldg(bt_row + pg);
-      if (static_cast<unsigned>(id) >= static_cast<unsigned>(num_pages)) {
-        record_error(status, PA_ERR_BAD_BLOCK);
-        id = 0;
-      }
-    }
-    const int s = t & 1;
-    bool stop = false;
-    for (int which = 0; which < 2 && !stop; ++which) {  // K, then V
-      if (t >= 2) {
-        const int fb = (which ? kBarVFree : kBarKFree) + s;
-        if (!__all_sync(kFull, mbar_wait(bar(fb), ((t - 2) >> 1) & 1)) || *abort_flag) {
-          stop = true;
-          break;
-        }
-      }
-      const uint32_t full = bar((which ? kBarV : kBarK) + s);
-      const uint32_t dst0 = sb + (which ? L::kV0 : L::kK0) + s * L::kKVBytes;
-      if (lane == 0) mbar_arrive_expect_tx(full, L::kKVBytes);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int idj = __shfl_sync(kFull, id, j);
-        if (lane == 0) {
-          const int y = idj * y_page + y_head;
-#pragma unroll
-          for (int bx = 0; bx < kBoxes; ++bx)
-            tma_load_2d(dst0 + bx * L::kColBlk + j * 2048, which ? vmap : kmap, bx * 64, y,
-                        full);
-        }
-      }
-      issued[which] = t + 1;
-    }
-    if (stop) break;
-  }
-  // Every issued copy lands before the CTA can leave (consumers wait for them
-  // on the normal path; this covers an aborted one).
-  for (int which = 0; which < 2; ++which)
-    for (int t = issued[which] >= 2 ? issued[which] - 2 : 0; t < issued[which]; ++t)
-      mbar_wait(bar((which ? kBarV : kBarK) + (t & 1)), (t >> 1) & 1);
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Bounded wait on one mbarrier phase that also gives up once another role has
+// raised the abort flag.  Warp-wide callers combine the result with
+// __all_sync.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int *abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
+__device__ __forceinline__ void raise_abort(int *status, volatile int *abort_flag) {
+  record_error(status, PA_ERR_TIMEOUT);
+  *abort_flag = 1;
+}
+
+// Load warp: K_t and V_t into stage t % kStages, each once the MMAs that
+// read the stage's previous tile have completed.  Lane j < 8 copies page j
+// of the tile (one box per 64 columns).  Page ids come in 32-page windows
+// held one per lane, fetched one window ahead and checked when used.
+template <int D>
+__device__ __forceinline__ void load_tiles(const CUtensorMap *kmap, const CUtensorMap *vmap,
+                                           uint32_t sb, const int32_t *bt_row, int n_pages,
+                                           int n_tiles, int num_pages, int y_page, int y_head,
+                                           int *status, volatile int *abort_flag, int lane) {
+  using L = TcSmem<D>;
+  constexpr int S = L::kStages;
+  constexpr int kBoxes = D / 64;
+  auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
+  auto load_window = [&](int w) {
+    const int pg = 32 * w + lane;
+    return pg < n_pages ? __ldg(bt_row + pg) : 0;  // past the end: page 0, masked
+  };
+  if (lane == 0) {
+    prefetch_tensormap(kmap);
+    prefetch_tensormap(vmap);
+  }
+  int wcur = load_window(0), wnext = load_window(1);
+  auto load_tile = [&](int which, int t, int idj) {
+    const int s = t % S;
+    const uint32_t full = bar((which ? kBarV : kBarK) + s);
+    const uint32_t dst0 = sb + (which ? L::kV0 : L::kK0) + s * L::kKVBytes;
+    if (lane == 0) mbar_arrive_expect_tx(full, L::kKVBytes);
+    __syncwarp();
+    if (lane < 8) {
+#pragma unroll
+      for (int bx = 0; bx < kBoxes; ++bx)
+        tma_load_2d(dst0 + bx * L::kColBlk + lane * 2048, which ? vmap : kmap, bx * 64,
+                    idj * y_page + y_head, full);
+    }
+  };
+  int issued = 0;
+  bool failed = false;
+  for (int t = 0; t < n_tiles; ++t) {
+    if (t > 0 && (t & 3) == 0) {  // the tile starts a new 32-page window
+      wcur = wnext;
+      wnext = load_window((t >> 2) + 1);
+    }
+    int idj = __shfl_sync(kFull, wcur, 8 * (t & 3) + (lane & 7));
+    if (lane < 8 && static_cast<unsigned>(idj) >= static_cast<unsigned>(num_pages)) {
+      record_error(status, PA_ERR_BAD_BLOCK);
+      idj = 0;
+    }
+    const int par = ((t / S) - 1) & 1;
+    if (t >= S && !__all_sync(kFull, wait_or_abort(bar(kBarKFree + t % S), par, abort_flag))) {
+      failed = true;
+      break;
+    }
+    load_tile(0, t, idj);
+    if (t >= S && !__all_sync(kFull, wait_or_abort(bar(kBarVFree + t % S), par, abort_flag))) {
+      issued = 2 * t + 1;
+      failed = true;
+      break;
+    }
+    load_tile(1, t, idj);
+    issued = 2 * t + 2;
+  }
+  if (failed) {
+    if (lane == 0) raise_abort(status, abort_flag);
+    // Copies in flight still land in shared memory: wait for them.
+    for (int i = issued - 1; i >= 0 && i >= issued - 2 * S; --i) {
+      const int t = i >> 1;
+      mbar_wait(bar(((i & 1) ? kBarV : kBarK) + t % S), (t / S) & 1);
+    }
+  }
+}
+
+// MMA warp (lane 0 issues): S_0, S_1, then per tile t
+//   O_0 += P_t V_t (keys 0-63), O_1 += P_t V_t (keys 64-127), S_{t+2}.
+// S_{t+2} goes after P V_t because it overwrites P_t in TMEM buffer t&1;
+// tcgen05 MMAs of one thread run in issue order.
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_tiles(uint32_t sb, uint32_t tS, uint32_t tO, int n_tiles,
+                                          int *status, volatile int *abort_flag, int lane) {
+  using L = TcSmem<D>;
+  constexpr int S = L::kStages;
+  constexpr int KSQ = D / 16;
+  constexpr uint32_t kIdS = tc::idesc_f16(BF16, kRows, kKeys, false, false);
+  constexpr uint32_t kIdO = tc::idesc_f16(BF16, kRows, D, false, true);
+  auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
+  // Descriptors of stage 0 / the Q tile; other stages and K steps add their
+  // byte offset >> 4 to the address field.
+  const uint64_t dq = tc::smem_desc_sw128(sb + L::kQ, 16, 1024);
+  const uint64_t dk = tc::smem_desc_sw128(sb + L::kK0, 16, 1024);
+  const uint64_t dv = tc::smem_desc_sw128(sb + L::kV0, L::kColBlk, 1024);
+  uint32_t last_bar = 0, last_par = 0;  // most recent commit (for the failure path)
+  bool failed = false;
+
+  auto issue_s = [&](int t) {
+    if (!__all_sync(kFull, wait_or_abort(bar(kBarK + t % S), (t / S) & 1, abort_flag)))
+      return false;
+    tc::fence_after_sync();
+    if (lane == 0) {
+      const uint64_t kst = dk + static_cast<uint64_t>((t % S) * L::kKVBytes >> 4);
+#pragma unroll
+      for (int kk = 0; kk < KSQ; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kColBlk + (kk & 3) * 32) >> 4);
+        tc::mma_f16(tS + (t & 1) * kKeys, dq + off, kst + off, kIdS, kk > 0);
+      }
+      tc::commit(bar(kBarS + (t & 1)));
+      tc::commit(bar(kBarKFree + t % S));
+    }
+    __syncwarp();
+    last_bar = bar(kBarS + (t & 1));
+    last_par = (t >> 1) & 1;
+    return true;
+  };
+  auto issue_pv = [&](int t, int h) {
+    if (!__all_sync(kFull, wait_or_abort(bar(kBarPReady + h), t & 1, abort_flag))) return false;
+    if (h == 0 &&
+        !__all_sync(kFull, wait_or_abort(bar(kBarV + t % S), (t / S) & 1, abort_flag)))
+      return false;
+    tc::fence_after_sync();
+    if (lane == 0) {
+      const uint64_t vst = dv + static_cast<uint64_t>((t % S) * L::kKVBytes >> 4);
+      const uint32_t pa = tS + (t & 1) * kKeys + 64 * h;  // this half's P: hi, then lo
+#pragma unroll
+      for (int ph = 0; ph < 2; ++ph) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_f16_tmem_a(tO + h * D, pa + 32 * ph + 8 * kk,
+                             vst + static_cast<uint64_t>(((4 * h + kk) * 2048) >> 4), kIdO,
+                             (t > 0 || kk > 0 || ph > 0) ? 1u : 0u);
+      }
+      tc::commit(bar(kBarO + h));
+      if (h == 1) tc::commit(bar(kBarVFree + t % S));
+    }
+    __syncwarp();
+    last_bar = bar(kBarO + h);
+    last_par = t & 1;
+    return true;
+  };
+
+  bool any = false;
+  if (!issue_s(0)) failed = true;
+  else any = true;
+  if (!failed && n_tiles > 1 && !issue_s(1)) failed = true;
+  for (int t = 0; t < n_tiles && !failed; ++t) {
+    if (!issue_pv(t, 0) || !issue_pv(t, 1) || (t + 2 < n_tiles && !issue_s(t + 2)))
+      failed = true;
+  }
+  if (failed) {
+    if (lane == 0) raise_abort(status, abort_flag);
+    // Nothing this warp started may still run when the CTA leaves.
+    if (any) mbar_wait(last_bar, last_par);
+  }
+}
+
+// Consumer warps 0-7: threads r and r + 128 share row r % 128; warps w and
+// w + 4 reach the same TMEM lanes.  `half` owns keys [64 half, 64 half + 64)
+// of every tile, with its own running (m, l) and its own accumulator O_half.
 template <int D, int GT, bool BF16>
 __device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t tO,
                                               const TcParams &p, int b, int q0, int hbase,
                                               int nq, int ctx, int kmax, int n_tiles,
                                               volatile int *abort_flag, int tid, int warp,
-                                              int lane);
+                                              int lane) {
+  using L = TcSmem<D>;
+  constexpr int S = L::kStages;
+  constexpr int HK = kKeys / 2;  // keys of each tile this thread owns
+  auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
+  const int half = warp >> 2;
+  const int r = ((warp & 3) << 5) + lane, qi = r / GT, hh = r % GT;
+  const int lim = min(ctx + q0 + qi, kmax);  // last key row r sees
+  const int lim_all = ctx + q0;              // every row sees keys <= this
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tOh = tO + half * D + lane_base;  // this half's accumulator row
 
-// Consumer warps 0-7 (threads r and r + 128 share row r % 128); thread 0 also
-// issues the MMAs.  Warp 8 produces the K/V tiles.
+  bool bad = false;
+  float m = -INFINITY, l = 0.f;
+  for (int j = 0; j < n_tiles; ++j) {
+    const int key0 = j * kKeys;
+    const int kbase = key0 + half * HK;
+    // my 64 columns of buffer j&1: S_j, then P_j (head terms, remainder terms)
+    const uint32_t tSj = tS + (j & 1) * kKeys + half * HK + lane_base;
+    if (!__all_sync(kFull, wait_or_abort(bar(kBarS + (j & 1)), (j >> 1) & 1, abort_flag))) {
+      bad = true;
+      break;
+    }
+    tc::fence_after_sync();
+    uint32_t sr[HK];
+    tc::ld32(tSj, *reinterpret_cast<uint32_t(*)[32]>(sr));
+    tc::ld32(tSj + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+    tc::wait_ld();
+
+    // ---- scale, mask, max of my keys; lazy move of my reference max
+    float tmax = -INFINITY;
+    if (key0 + kKeys - 1 <= lim_all) {  // no key of this tile is masked
+#pragma unroll
+      for (int c = 0; c < HK; ++c) {
+        const float v = __uint_as_float(sr[c]) * p.qscale;
+        sr[c] = __float_as_uint(v);
+        tmax = fmaxf(tmax, v);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < HK; ++c) {
+        const float v = (kbase + c <= lim) ? __uint_as_float(sr[c]) * p.qscale : -INFINITY;
+        sr[c] = __float_as_uint(v);
+        tmax = fmaxf(tmax, v);
+      }
+    }
+    const bool need = tmax > m + kSlack;
+    float corr = 1.f;
+    if (need) {
+      const float mn = fmaxf(m, tmax);
+      corr = ex2(m - mn);  // 0 while m was still -inf
+      m = mn;
+      l *= corr;
+    }
+    // ---- P = e^(s - m) as head + remainder, into the columns S_j came from
+    const bool live = m != -INFINITY;  // nothing seen yet: every weight is 0
+    {
+      uint32_t phi[HK / 2], plo[HK / 2];
+#pragma unroll
+      for (int k = 0; k < HK / 2; ++k) {
+        const float p0 = live ? ex2(__uint_as_float(sr[2 * k]) - m) : 0.f;
+        const float p1 = live ? ex2(__uint_as_float(sr[2 * k + 1]) - m) : 0.f;
+        l += p0 + p1;
+        phi[k] = pack2<BF16>(p0, p1);
+        const float2 hr = unpack2<BF16>(phi[k]);
+        plo[k] = pack2<BF16>(p0 - hr.x, p1 - hr.y);
+      }
+      tc::st32(tSj, phi);
+      tc::st32(tSj + 32, plo);
+    }
+    // ---- P V_{j-1} of my half done: my accumulator is stable (and the MMA
+    // warp has taken P_{j-1}, so this warp's next arrival starts a new phase)
+    if (j > 0) {
+      if (!__all_sync(kFull, wait_or_abort(bar(kBarO + half), (j - 1) & 1, abort_flag))) {
+        bad = true;
+        break;
+      }
+      tc::fence_after_sync();
+      if (__any_sync(kFull, need)) {
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t o[32];
+          tc::ld32(tOh + cb * 32, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
+          tc::st32(tOh + cb * 32, o);
+        }
+      }
+    }
+    tc::wait_st();
+    // ---- V rows past the last key any row sees may hold non-finite junk;
+    // P is 0 there but 0 * inf is NaN inside the MMA, so clear them (each half
+    // clears the rows its own P V reads).
+    if (key0 + kKeys - 1 > kmax) {
+      if (!__all_sync(kFull, wait_or_abort(bar(kBarV + j % S), (j / S) & 1, abort_flag))) {
+        bad = true;
+        break;
+      }
+      const uint32_t vst = sb + L::kV0 + (j % S) * L::kKVBytes;
+      const int first = max(kmax - key0 + 1, half * HK);
+      const int htid = tid & (kConsumers / 2 - 1);
+      for (int e = htid; e < (half * HK + HK - first) * (D / 8); e += kConsumers / 2) {
+        const int rr = first + e / (D / 8), c = e % (D / 8);
+        st_shared_v4(vst + (c >> 3) * L::kColBlk + swz128(rr, c), 0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();  // cleared V rows -> read by the tensor cores
+    }
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kBarPReady + half));  // one arrival per warp
+  }
+  tc::wait_st();
+  if (!bad)
+    bad = !__all_sync(kFull, wait_or_abort(bar(kBarO), (n_tiles - 1) & 1, abort_flag));
+  if (!bad)
+    bad = !__all_sync(kFull, wait_or_abort(bar(kBarO + 1), (n_tiles - 1) & 1, abort_flag));
+  tc::fence_after_sync();
+
+  // ---- merge the two halves once (exponent law) and write O / l.  Every
+  // K/V copy has landed and been read by now, so K stage 0 carries the
+  // exchange.
+  const uint32_t x_mine = sb + L::kK0 + (half * kRows + r) * 8;
+  const uint32_t x_peer = sb + L::kK0 + ((half ^ 1) * kRows + r) * 8;
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(x_mine), "f"(m), "f"(l) : "memory");
+  if (consumers_sync_or(bad)) {
+    if (tid == 0) raise_abort(p.status, abort_flag);
+    return;
+  }
+  float m2, l2;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(m2), "=f"(l2) : "r"(x_peer) : "memory");
+  const float mA = half ? m2 : m, lA = half ? l2 : l;  // keys [0, 64) of each tile
+  const float mB = half ? m : m2, lB = half ? l : l2;  // keys [64, 128)
+  const float M = fmaxf(mA, mB);
+  const float fA = mA == -INFINITY ? 0.f : ex2(mA - M);
+  const float fB = mB == -INFINITY ? 0.f : ex2(mB - M);
+  const float lt = lA * fA + lB * fB;
+  const float sA = lt > 0.f ? fA / lt : 0.f, sB = lt > 0.f ? fB / lt : 0.f;
+  float *dst = p.out +
+               ((static_cast<size_t>(b) * p.n_new + q0 + qi) * p.n_q_heads + hbase + hh) * D +
+               half * (D / 2);
+#pragma unroll
+  for (int cb = 0; cb < D / 64; ++cb) {  // my D/2 output columns
+    uint32_t oa[32], ob[32];
+    tc::ld32(tO + lane_base + half * (D / 2) + cb * 32, oa);
+    tc::ld32(tO + D + lane_base + half * (D / 2) + cb * 32, ob);
+    tc::wait_ld();
+    if (qi < nq) {
+#pragma unroll
+      for (int k = 0; k < 32; k += 4)
+        *reinterpret_cast<float4 *>(dst + cb * 32 + k) = make_float4(
+            __uint_as_float(oa[k]) * sA + __uint_as_float(ob[k]) * sB,
+            __uint_as_float(oa[k + 1]) * sA + __uint_as_float(ob[k + 1]) * sB,
+            __uint_as_float(oa[k + 2]) * sA + __uint_as_float(ob[k + 2]) * sB,
+            __uint_as_float(oa[k + 3]) * sA + __uint_as_float(ob[k + 3]) * sB);
+    }
+  }
+}
+
 template <int D, int GT, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const TcParams p) {
   using L = TcSmem<D>;
-  constexpr int BQ = kRows / GT;   // queries per CTA
+  constexpr int BQ = kRows / GT;  // queries per CTA
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -196,12 +498,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kSlot + 4);
 
   if (tid == 0) {
-    for (int i = 0; i < 10; ++i) mbar_init(bar(i), 1);
+    for (int i = 0; i < kNumBars; ++i)
+      mbar_init(bar(i), (i == kBarPReady || i == kBarPReady + 1) ? kConsumers / 64 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    tc::alloc(sb + L::kSlot, 256);  // S: columns 0-127, O: 128 .. 128+D-1
+    // S_0: columns 0-127, S_1: 128-255, O_A: 256 .. 256+D-1, O_B: 256+D .. 256+2D-1
+    tc::alloc(sb + L::kSlot, 512);
     tc::relinquish();
   }
   // Q tile: row r = query r / GT, head r % GT (zeros past the chunk's end)
@@ -222,12 +526,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kSlot);
-  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t tS = tmem, tO = tmem + 2 * kKeys;
 
-  if (warp == kConsumers / 32) {
-    produce_tiles<D>(&kmap, &vmap, sb, p.block_table + static_cast<size_t>(b) * p.max_blocks,
-                     n_pages, n_tiles, p.num_pages, p.n_kv_heads * 16, g * 16, p.status,
-                     abort_flag, lane);
+  if (warp == kLoadWarp) {
+    load_tiles<D>(&kmap, &vmap, sb, p.block_table + static_cast<size_t>(b) * p.max_blocks,
+                  n_pages, n_tiles, p.num_pages, p.n_kv_heads * 16, g * 16, p.status,
+                  abort_flag, lane);
+  } else if (warp == kMmaWarp) {
+    mma_tiles<D, BF16>(sb, tS, tO, n_tiles, p.status, abort_flag, lane);
   } else {
     consume_tiles<D, GT, BF16>(sb, tS, tO, p, b, q0, hbase, nq, ctx, kmax, n_tiles,
                                abort_flag, tid, warp, lane);
@@ -236,210 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc::fence_after_sync();
-    tc::dealloc(tmem, 256);
-  }
-}
-
-__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-template <int D, int GT, bool BF16>
-__device__ __forceinline__ void consume_tiles(uint32_t sb, uint32_t tS, uint32_t tO,
-                                              const TcParams &p, int b, int q0, int hbase,
-                                              int nq, int ctx, int kmax, int n_tiles,
-                                              volatile int *abort_flag, int tid, int warp,
-                                              int lane) {
-  using L = TcSmem<D>;
-  constexpr int KSQ = D / 16;
-  constexpr int HK = kKeys / 2;  // S columns (keys) per thread
-  constexpr int HD = D / 2;      // O columns per thread
-  constexpr uint32_t kIdS = tc::idesc_f16(BF16, kRows, kKeys, false, false);
-  constexpr uint32_t kIdO = tc::idesc_f16(BF16, kRows, D, false, true);
-  auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
-  // Two threads per row: warps w and w + 4 reach the same TMEM lanes; `half`
-  // picks keys [64 half, 64 half + 64) of S and columns [HD half, +HD) of O.
-  const int half = warp >> 2;
-  const int r = ((warp & 3) << 5) + lane, qi = r / GT, hh = r % GT;
-  const int lim = min(ctx + q0 + qi, kmax);  // last key row r sees
-  const int lim_all = ctx + q0;              // every row sees keys <= this
-  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const uint32_t x_mine = sb + L::kXchg + (half * kRows + r) * 4;
-  const uint32_t x_peer = sb + L::kXchg + ((half ^ 1) * kRows + r) * 4;
-  int issued_s = 0, issued_o = 0;  // thread 0's MMA groups, for a drain on error
-
-  auto issue_s = [&](int t) {  // S_t = Q K_t^T, one thread
-    const uint32_t kst = sb + L::kK0 + (t & 1) * L::kKVBytes;
-#pragma unroll
-    for (int kk = 0; kk < KSQ; ++kk) {
-      const uint32_t off = (kk >> 2) * L::kColBlk + (kk & 3) * 32;
-      tc::mma_f16(tS, tc::smem_desc_sw128(sb + L::kQ + off, 16, 1024),
-                  tc::smem_desc_sw128(kst + off, 16, 1024), kIdS, kk > 0);
-    }
-    tc::commit(bar(kBarS));
-    tc::commit(bar(kBarKFree + (t & 1)));
-    ++issued_s;
-  };
-  auto issue_pv = [&](int t) {  // O += P_hi V_t + P_lo V_t, one thread
-    const uint32_t vst = sb + L::kV0 + (t & 1) * L::kKVBytes;
-#pragma unroll
-    for (int ph = 0; ph < 2; ++ph) {
-      const uint32_t pb = sb + (ph ? L::kPlo : L::kPhi);
-#pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk)
-        tc::mma_f16(tO, tc::smem_desc_sw128(pb + (kk >> 2) * L::kColBlk + (kk & 3) * 32, 16, 1024),
-                    tc::smem_desc_sw128(vst + kk * 2048, L::kColBlk, 1024), kIdO,
-                    (t > 0 || kk > 0 || ph > 0) ? 1u : 0u);
-    }
-    tc::commit(bar(kBarO));
-    tc::commit(bar(kBarVFree + (t & 1)));
-    ++issued_o;
-  };
-
-  bool bad = false;
-  if (tid == 0) {
-    if (mbar_wait(bar(kBarK), 0)) issue_s(0);
-    else bad = true;
-  }
-  float m = -INFINITY, l = 0.f;
-  for (int j = 0; j < n_tiles; ++j) {
-    const int key0 = j * kKeys;
-    const int kbase = key0 + half * HK;
-    // ---- my half of S_j's row -> registers, scaled and masked, half max
-    if (!mbar_wait(bar(kBarS), j & 1)) bad = true;
-    tc::fence_after_sync();
-    uint32_t sr[HK];
-#pragma unroll
-    for (int cb = 0; cb < HK / 32; ++cb)
-      tc::ld32(tS + lane_base + half * HK + cb * 32,
-               *reinterpret_cast<uint32_t(*)[32]>(sr + cb * 32));
-    tc::wait_ld();
-    float hmax = -INFINITY;
-    if (key0 + kKeys - 1 <= lim_all) {  // no key of this tile is masked
-#pragma unroll
-      for (int c = 0; c < HK; ++c) {
-        const float v = __uint_as_float(sr[c]) * p.qscale;
-        sr[c] = __float_as_uint(v);
-        hmax = fmaxf(hmax, v);
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < HK; ++c) {
-        const float v = (kbase + c <= lim) ? __uint_as_float(sr[c]) * p.qscale : -INFINITY;
-        sr[c] = __float_as_uint(v);
-        hmax = fmaxf(hmax, v);
-      }
-    }
-    st_shared_f32(x_mine, hmax);
-    tc::fence_before_sync();
-    if (consumers_sync_or(bad)) { bad = true; break; }  // S buffer, K stage free
-    if (tid == 0 && j + 1 < n_tiles) {
-      tc::fence_after_sync();
-      if (mbar_wait(bar(kBarK + ((j + 1) & 1)), ((j + 1) >> 1) & 1)) issue_s(j + 1);
-      else bad = true;
-    }
-
-    // ---- row max from both halves; lazy rescale decision (same in both)
-    const float tmax = fmaxf(hmax, ld_shared_f32(x_peer));
-    const bool need = tmax > m + kSlack;
-    float corr = 1.f;
-    if (need) {
-      const float mn = fmaxf(m, tmax);
-      corr = ex2(m - mn);  // 0 on the first tile (m = -inf)
-      m = mn;
-      l *= corr;
-    }
-    // ---- P V_{j-1} done: O is stable and the P buffers are free
-    if (j > 0) {
-      if (!mbar_wait(bar(kBarO), (j - 1) & 1)) bad = true;
-      tc::fence_after_sync();
-      if (__any_sync(kFull, need)) {
-#pragma unroll
-        for (int cb = 0; cb < HD / 32; ++cb) {
-          uint32_t o[32];
-          tc::ld32(tO + lane_base + half * HD + cb * 32, o);
-          tc::wait_ld();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
-          tc::st32(tO + lane_base + half * HD + cb * 32, o);
-        }
-        tc::wait_st();
-      }
-    }
-    // ---- P = e^(s - m) as head + remainder: my 64 keys = 64-column block `half`
-#pragma unroll
-    for (int ch = 0; ch < HK / 8; ++ch) {
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float p0 = ex2(__uint_as_float(sr[ch * 8 + 2 * k]) - m);
-        const float p1 = ex2(__uint_as_float(sr[ch * 8 + 2 * k + 1]) - m);
-        l += p0 + p1;
-        hi[k] = pack2<BF16>(p0, p1);
-        const float2 hr = unpack2<BF16>(hi[k]);
-        lo[k] = pack2<BF16>(p0 - hr.x, p1 - hr.y);
-      }
-      const uint32_t off = half * L::kColBlk + swz128(r, ch);
-      st_shared_v4(sb + L::kPhi + off, hi[0], hi[1], hi[2], hi[3]);
-      st_shared_v4(sb + L::kPlo + off, lo[0], lo[1], lo[2], lo[3]);
-    }
-    // ---- V rows past the last key any row sees may hold non-finite junk;
-    // P is 0 there but 0 * inf is NaN inside the MMA, so clear them.
-    if (key0 + kKeys - 1 > kmax) {
-      if (!mbar_wait(bar(kBarV + (j & 1)), (j >> 1) & 1)) bad = true;
-      const uint32_t vst = sb + L::kV0 + (j & 1) * L::kKVBytes;
-      const int first = kmax - key0 + 1;
-      for (int e = tid; e < (kKeys - first) * (D / 8); e += kConsumers) {
-        const int rr = first + e / (D / 8), c = e % (D / 8);
-        st_shared_v4(vst + (c >> 3) * L::kColBlk + swz128(rr, c), 0u, 0u, 0u, 0u);
-      }
-    }
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    if (consumers_sync_or(bad)) { bad = true; break; }
-    if (tid == 0) {
-      tc::fence_after_sync();
-      if (mbar_wait(bar(kBarV + (j & 1)), (j >> 1) & 1)) issue_pv(j);
-      else bad = true;
-    }
-  }
-
-  // ---- O / l, one write per row (each thread its HD columns)
-  if (!bad && !mbar_wait(bar(kBarO), (n_tiles - 1) & 1)) bad = true;
-  tc::fence_after_sync();
-  st_shared_f32(x_mine, l);
-  if (consumers_sync_or(bad)) {
-    if (tid == 0) {
-      record_error(p.status, PA_ERR_TIMEOUT);
-      *abort_flag = 1;
-      // let the MMAs in flight finish before the tensor memory is freed
-      if (issued_s) mbar_wait(bar(kBarS), (issued_s - 1) & 1);
-      if (issued_o) mbar_wait(bar(kBarO), (issued_o - 1) & 1);
-    }
-    return;
-  }
-  const float lt = l + ld_shared_f32(x_peer);
-  const float inv = lt > 0.f ? 1.f / lt : 0.f;
-  float *dst = p.out +
-               ((static_cast<size_t>(b) * p.n_new + q0 + qi) * p.n_q_heads + hbase + hh) * D +
-               half * HD;
-#pragma unroll
-  for (int cb = 0; cb < HD / 32; ++cb) {
-    uint32_t o[32];
-    tc::ld32(tO + lane_base + half * HD + cb * 32, o);
-    tc::wait_ld();
-    if (qi < nq) {
-#pragma unroll
-      for (int k = 0; k < 32; k += 4)
-        *reinterpret_cast<float4 *>(dst + cb * 32 + k) =
-            make_float4(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
-                        __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
-    }
+    tc::dealloc(tmem, 512);
   }
 }
 

@@ -381,7 +381,7 @@ def run_prefill(torch, pa, workloads, steps, warmup, peaks):
     peak = peaks.get("bf16_tflops", 1900.0)
     res = {"ms": round(ms, 4), "TFLOP_s": round(tf, 1), "flops": fl,
            "frac_of_bf16_peak": round(tf / peak, 4), "peak_tflops": peak,
-           "kernel": "tcgen05.mma (TMEM accumulators), M=128 rows per CTA",
+           "kernel": "prefill_tc_kernel: tcgen05.mma, two 128-row tiles per CTA, P and O in TMEM",
            "l2": "flushed (2x L2 write) before each call"}
     del case, out
     torch.cuda.empty_cache()

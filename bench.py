@@ -326,24 +326,36 @@ def run_other_decode(torch, pa, workloads, name, steps, warmup, partition_tokens
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
-    times = []
-    for _ in range(steps):
-        if flush is not None:
+    if flush is not None:
+        # each step after a flush, timed alone (median)
+        times = []
+        for _ in range(steps):
             flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+    else:
+        # steps back to back between one pair of events: the device time per
+        # step, without the host's per-call latency of a short step
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        step()
+        for _ in range(steps):
+            step()
         b.record(stream)
         torch.cuda.synchronize()
-        times.append(a.elapsed_time(b))
+        ms = a.elapsed_time(b) / steps
     assert pa.pa_last_device_error() == 0
-    ms = statistics.median(times)
     gbs = L * per_layer / (ms * 1e-3) / 1e9
     res = {"ms_per_step": round(ms, 4), "GB_s": round(gbs, 1),
            "seq_layers_per_s": round(L * B / (ms * 1e-3), 1),
            "partition_tokens": part, "bytes_per_step": L * per_layer,
-           "l2": "flushed (2x L2 write) before each step" if flush is not None
-           else "inputs larger than 2x L2, no flush"}
+           "l2": "flushed (2x L2 write) before each step, each step timed alone"
+           if flush is not None
+           else "inputs larger than 2x L2, no flush; steps timed back to back"}
     del case, out, ws
     torch.cuda.empty_cache()
     return res

@@ -297,10 +297,14 @@ __device__ __forceinline__ bool pages_cuda_core(Ring &ring, int i_begin, int i_e
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core page loop (GT >= 2).  Row r = lane / 4 of the accumulators is
-// query head r of the tile (rows >= GT are padding); this lane holds keys
-// k0, k0+1, k0+8, k0+9 of the page (k0 = 2 * (lane % 4)) and output dims
-// 8n + k0, 8n + k0 + 1.
+// Tensor-core page loop (GT >= 2).  Row r = lane / 4 of the score
+// accumulators is query head r of the tile (rows >= GT are padding); this
+// lane holds keys k0, k0+1, k0+8, k0+9 of the page (k0 = 2 * (lane % 4)).
+// In P V the A operand's rows 0-7 carry the 16-bit head terms of P and rows
+// 8-15 (padding in S) the remainder terms, so one MMA does both: o[n][0..1]
+// accumulate head r's output dims 8n + k0, 8n + k0 + 1 from the head terms,
+// o[n][2..3] the same dims from the remainders; the two are summed when the
+// state leaves registers.
 template <int D, int GT, bool BF16, int NW, int S, class Ring>
 __device__ __forceinline__ bool pages_mma(Ring &ring, int i_begin, int i_end,
                                           const CUtensorMap *kmap,
@@ -368,6 +372,8 @@ __device__ __forceinline__ bool pages_mma(Ring &ring, int i_begin, int i_end,
       for (int n = 0; n < NT; ++n) {
         o[n][0] *= c;
         o[n][1] *= c;
+        o[n][2] *= c;
+        o[n][3] *= c;
       }
     }
     float p[4];
@@ -376,17 +382,15 @@ __device__ __forceinline__ bool pages_mma(Ring &ring, int i_begin, int i_end,
     l_r += (p[0] + p[1]) + (p[2] + p[3]);
     const uint32_t h01 = pack2<BF16>(p[0], p[1]), h89 = pack2<BF16>(p[2], p[3]);
     const float2 r01 = unpack2<BF16>(h01), r89 = unpack2<BF16>(h89);
-    const uint32_t pa[4] = {h01, 0u, h89, 0u};
-    const uint32_t pb[4] = {pack2<BF16>(p[0] - r01.x, p[1] - r01.y), 0u,
-                            pack2<BF16>(p[2] - r89.x, p[3] - r89.y), 0u};
+    // rows 0-7: head terms, rows 8-15: remainders of the same weights
+    const uint32_t pa[4] = {h01, pack2<BF16>(p[0] - r01.x, p[1] - r01.y), h89,
+                            pack2<BF16>(p[2] - r89.x, p[3] - r89.y)};
 #pragma unroll
     for (int nn = 0; nn < NT / 2; ++nn) {
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(st + Ring::kPageBytes + swz(rv, 2 * nn + (lane >> 4), 16), b0, b1, b2, b3);
       mma16816<BF16>(o[2 * nn], pa, b0, b1);
       mma16816<BF16>(o[2 * nn + 1], pa, b2, b3);
-      mma16816<BF16>(o[2 * nn], pb, b0, b1);
-      mma16816<BF16>(o[2 * nn + 1], pb, b2, b3);
     }
     __syncwarp();
     if (i + S < ring.n_i) ring.issue(i + S, lane, kmap, vmap);
@@ -526,7 +530,8 @@ __global__ void __launch_bounds__(NW * 32)
           float *dst = p.ws + ((row0 + r) * p.n_parts + part) * (D + 4);
 #pragma unroll
           for (int n = 0; n < D / 8; ++n)
-            *reinterpret_cast<float2 *>(dst + n * 8 + k0) = make_float2(o[n][0], o[n][1]);
+            *reinterpret_cast<float2 *>(dst + n * 8 + k0) =
+                make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
           if ((lane & 3) == 0) *reinterpret_cast<float2 *>(dst + D) = make_float2(m_r * kLn2, l_r);
         }
         if (!ok) break;
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
       for (int n = 0; n < D / 8; ++n)
         *reinterpret_cast<float2 *>(mer_o + (warp * GT + r) * D + n * 8 + k0) =
-            make_float2(o[n][0], o[n][1]);
+            make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
     }
   } else {
     constexpr int DPL = D / 32;
@@ -634,21 +639,20 @@ __global__ void __launch_bounds__(NW * 32)
 // ---------------------------------------------------------------------------
 // Exact merge of partition states (the exponent law: M = max m_p,
 // l = sum e^(m_p - M) l_p, o = sum e^(m_p - M) O_p / l), one CTA of 128
-// threads per (sequence, head).  Every load of a pass is independent of the
-// others, so a row costs a few memory round trips however many partitions:
-// pass 1 reduces M and l over the partitions' (m, l) pairs; pass 2 gives each
-// thread a float4 of head_dim and every SL-th partition; the SL slices are
-// summed through shared memory.
+// threads per (sequence, head).  Thread (sl, qd) owns a float4 of head_dim
+// and every SL-th partition, and folds its partitions into a running
+// (m, l, O) with the same law as it reads them, so all its loads are
+// independent and a row costs about one memory round trip; the SL slices
+// then fold through shared memory.
 template <int D>
 __global__ void __launch_bounds__(128)
     merge_kernel(const float *__restrict__ parts, const int32_t *__restrict__ ctx,
                  float *__restrict__ out, int *status, int n_q_heads, int n_parts,
                  int part_tokens) {
   constexpr int W = D + 4, Q = D / 4, SL = 128 / Q;
-  __shared__ float red[4];
+  __shared__ float2 sml[SL];
   __shared__ __align__(16) float sacc[SL][D];
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
   griddep_release();
   griddep_wait();
   long T = ctx[b];
@@ -664,58 +668,46 @@ __global__ void __launch_bounds__(128)
   const size_t row = static_cast<size_t>(b) * n_q_heads + h;
   const float *base = parts + row * static_cast<size_t>(n_parts) * W;
 
-  auto block_reduce = [&](float v, bool is_max) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float u = __shfl_xor_sync(0xffffffffu, v, o);
-      v = is_max ? fmaxf(v, u) : v + u;
-    }
-    __syncthreads();  // red[] is free
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    return is_max ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]))
-                  : (red[0] + red[1]) + (red[2] + red[3]);
-  };
-  float mloc = -INFINITY;
-  for (int q = tid; q < n_valid; q += 128) {
-    const float2 ml = __ldg(reinterpret_cast<const float2 *>(base + static_cast<size_t>(q) * W + D));
-    if (ml.y > 0.f) mloc = fmaxf(mloc, ml.x);
-  }
-  const float M = block_reduce(mloc, true);
-  float lloc = 0.f;
-  if (M != -INFINITY)
-    for (int q = tid; q < n_valid; q += 128) {
-      const float2 ml = __ldg(reinterpret_cast<const float2 *>(base + static_cast<size_t>(q) * W + D));
-      if (ml.y > 0.f) lloc += ex2((ml.x - M) * kLog2e) * ml.y;
-    }
-  const float lt = block_reduce(lloc, false);
-
   const int qd = tid % Q, sl = tid / Q;
+  float m = -INFINITY, l = 0.f;  // m in log2 units
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
 #pragma unroll 8
-    for (int q = sl; q < n_valid; q += SL) {
-      const float *sp = base + static_cast<size_t>(q) * W;
-      const float2 ml = __ldg(reinterpret_cast<const float2 *>(sp + D));
-      const float4 o4 = __ldg(reinterpret_cast<const float4 *>(sp) + qd);
-      const float f = ml.y > 0.f ? ex2((ml.x - M) * kLog2e) : 0.f;
-      acc.x += f * o4.x;
-      acc.y += f * o4.y;
-      acc.z += f * o4.z;
-      acc.w += f * o4.w;
+  for (int q = sl; q < n_valid; q += SL) {
+    const float *sp = base + static_cast<size_t>(q) * W;
+    const float2 ml = __ldg(reinterpret_cast<const float2 *>(sp + D));
+    const float4 o4 = __ldg(reinterpret_cast<const float4 *>(sp) + qd);
+    if (ml.y > 0.f) {  // an empty partition (l = 0) contributes nothing
+      const float mp = ml.x * kLog2e;
+      const float mn = fmaxf(m, mp);
+      const float a = ex2(m - mn), c = ex2(mp - mn);  // a = 0 while m = -inf
+      acc.x = acc.x * a + o4.x * c;
+      acc.y = acc.y * a + o4.y * c;
+      acc.z = acc.z * a + o4.z * c;
+      acc.w = acc.w * a + o4.w * c;
+      l = l * a + ml.y * c;
+      m = mn;
     }
   }
   *reinterpret_cast<float4 *>(&sacc[sl][4 * qd]) = acc;
+  if (qd == 0) sml[sl] = make_float2(m, l);
   __syncthreads();
   if (tid < Q) {
-    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < SL; ++k) {
-      const float4 v = *reinterpret_cast<const float4 *>(&sacc[k][4 * tid]);
-      t.x += v.x;
-      t.y += v.y;
-      t.z += v.z;
-      t.w += v.w;
+    for (int k = 0; k < SL; ++k) M = fmaxf(M, sml[k].x);
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lt = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int k = 0; k < SL; ++k) {
+        const float f = ex2(sml[k].x - M);  // 0 for a slice that saw nothing
+        const float4 v = *reinterpret_cast<const float4 *>(&sacc[k][4 * tid]);
+        t.x += f * v.x;
+        t.y += f * v.y;
+        t.z += f * v.z;
+        t.w += f * v.w;
+        lt += f * sml[k].y;
+      }
     }
     const float inv = lt > 0.f ? 1.f / lt : 0.f;
     reinterpret_cast<float4 *>(out + row * D)[tid] =

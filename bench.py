@@ -400,6 +400,63 @@ def run_prefill(torch, pa, workloads, steps, warmup, peaks):
     return res
 
 
+def run_verify(torch, pa, workloads, steps, warmup, peaks, gamma=4):
+    """Speculative-decoding verify at the 32k GQA-8 decode shape: 4 sequences
+    x 32768 cached tokens, 64/8 heads, gamma drafted tokens attended in one
+    pass (pa_prefill_paged_split, key ranges merged exactly).  HBM-bound like
+    decode: algorithmic bytes = unique K/V of ctx + gamma tokens + q + fp32
+    out.  The unsplit pa_prefill_paged is timed beside it."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, hq, hkv, D, ctx = 4, 64, 8, 128, 32768
+    case = workloads.paged_case(layers=1, batch=B, n_q_heads=hq, n_kv_heads=hkv,
+                                head_dim=D, page_size=16, ctx=[ctx] * B, dtype="bf16",
+                                seed=1006, n_new=gamma, kind="prefill", device=dev)
+    mb = case.block_table.shape[2]
+    part = pa.pa_prefill_partition_tokens(B, gamma, hq, hkv, D, 16, mb, 0)
+    ws_bytes = pa.pa_prefill_workspace_size(B, gamma, hq, hkv, D, 16, mb, 0)
+    ws = torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device=dev)
+    out = torch.empty((B, gamma, hq, D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    nbytes = (2 * (ctx + gamma) * hkv * D * 2) * B + B * gamma * hq * D * (2 + 4)
+
+    def time_it(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    def split():
+        pa.pa_prefill_paged_split(case.q[0], case.k_cache, case.v_cache, case.block_table[0],
+                                  case.ctx_lens, gamma, out, case.scale, hq, hkv, D, 16, B,
+                                  mb, case.k_cache.shape[0], case.dtype_code, 0, ws,
+                                  ws_bytes, stream.cuda_stream)
+
+    def unsplit():
+        pa.pa_prefill_paged(case.q[0], case.k_cache, case.v_cache, case.block_table[0],
+                            case.ctx_lens, gamma, out, case.scale, hq, hkv, D, 16, B, mb,
+                            case.k_cache.shape[0], case.dtype_code, stream.cuda_stream)
+
+    ms = time_it(split)
+    ms_unsplit = time_it(unsplit)
+    assert pa.pa_last_device_error() == 0
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res = {"ms_per_step": round(ms, 4), "GB_s": round(gbs, 1),
+           "frac_of_hbm_peak": round(gbs / peaks.get("hbm_gbs", 6800.0), 4),
+           "gamma": gamma, "partition_tokens": part, "bytes_per_step": nbytes,
+           "unsplit_ms": round(ms_unsplit, 4),
+           "kernel": "prefill_tc_kernel over key ranges + merge_kernel",
+           "l2": "inputs larger than 2x L2, no flush; steps timed back to back"}
+    del case, out, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_baseline_sample(torch, case, cfg, layers_budget_s=10.0):
     """The float64 oracle, as it stands, on whole layers of the headline
     workload until ~budget seconds pass (at least one layer)."""
@@ -513,6 +570,7 @@ def main_ours(args):
         other["mha_b1_ctx512"] = run_other_decode(torch, pa, workloads,
                                                   "mha_b1_ctx512", 20, 5)
         other["prefill_b4_512over8192"] = run_prefill(torch, pa, workloads, 10, 3, peaks)
+        other["verify_gamma4_b4_ctx32k"] = run_verify(torch, pa, workloads, 20, 3, peaks)
         for k, v in other.items():
             if "GB_s" in v:
                 v["frac_of_hbm_peak"] = round(v["GB_s"] / hbm, 4)

@@ -57,7 +57,8 @@ enum {
   PA_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than required */
   PA_ERR_ALIGN = -8,       /* a pointer not 16-byte aligned */
   PA_ERR_PARTITION = -9,   /* partition_tokens not 0 and not a positive
-                              multiple of page_size */
+                              multiple of page_size (decode) or of 128
+                              (pa_prefill_paged_split) */
   PA_ERR_CUDA = -10,       /* a CUDA runtime call or launch failed */
   PA_ERR_BAD_BLOCK = -11,  /* device: block-table entry outside [0, num_pages) */
   PA_ERR_BAD_CTX = -12,    /* device: context length < 0 or beyond the table */
@@ -185,6 +186,50 @@ int pa_prefill_paged(const void *q, const void *k_cache, const void *v_cache,
                      int n_kv_heads, int head_dim, int page_size, int batch,
                      int max_blocks_per_seq, int num_pages, pa_dtype dtype,
                      pa_stream_t stream);
+
+/*
+ * pa_prefill_paged_split -- pa_prefill_paged with each sequence's keys cut
+ * into partitions whose partial states (O, m, l) are merged exactly.
+ *
+ * Computes what pa_prefill_paged computes (same arguments, same result up to
+ * rounding order).  When there are few (query, head) row tiles -- a short
+ * chunk over a long context, and in particular the verify step of
+ * speculative decoding, where the gamma drafted tokens are attended in one
+ * pass with causal masking among themselves (ch. 19 "推理系统与性能工程",
+ * speculative sampling) -- a CTA per row tile leaves most SMs idle.  Here
+ * each CTA also takes one key range of partition_tokens keys, writes its
+ * rows' partial states, and a merge applies the exponent law of 19.6.2.
+ *   partition_tokens  0 = choose (see pa_prefill_partition_tokens), else a
+ *                     multiple of 128 (PA_ERR_PARTITION otherwise)
+ *   workspace         device float [batch][n_new][n_q_heads][n_parts]
+ *                     [head_dim + 4], 16-byte aligned, at least
+ *                     pa_prefill_workspace_size(...) bytes; owned by the
+ *                     caller, overwritten; may be NULL when that size is 0.
+ * Returns PA_ERR_WORKSPACE if the workspace is missing or too small.
+ */
+int pa_prefill_paged_split(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *ctx_lens,
+                           int n_new, float *out, float scale, int n_q_heads,
+                           int n_kv_heads, int head_dim, int page_size, int batch,
+                           int max_blocks_per_seq, int num_pages, pa_dtype dtype,
+                           int partition_tokens, void *workspace,
+                           size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * The key-range size pa_prefill_paged_split uses for these shapes (0 = no
+ * split), or a negative PA_ERR_* for invalid arguments.  The automatic
+ * choice splits only when there are fewer row-tile CTAs than SMs, into
+ * ranges of at least 512 keys, as many as keep the grid within two waves of
+ * one CTA per SM.
+ */
+int pa_prefill_partition_tokens(int batch, int n_new, int n_q_heads, int n_kv_heads,
+                                int head_dim, int page_size, int max_blocks_per_seq,
+                                int partition_tokens);
+
+/* Workspace bytes pa_prefill_paged_split needs (0 when it does not split). */
+size_t pa_prefill_workspace_size(int batch, int n_new, int n_q_heads, int n_kv_heads,
+                                 int head_dim, int page_size, int max_blocks_per_seq,
+                                 int partition_tokens);
 
 /*
  * pa_decode_static_workspace -- pa_decode for callers that cannot allocate.

@@ -21,7 +21,9 @@ __all__ = [
     "pa_decode_partition_tokens", "pa_decode_workspace_size",
     "pa_decode_static_workspace",
     "pa_merge_partials", "pa_append_kv", "pa_prefill_paged",
-    "pa_last_device_error", "pa_strerror", "decode", "prefill", "append_kv",
+    "pa_prefill_paged_split", "pa_prefill_partition_tokens", "pa_prefill_workspace_size",
+    "pa_last_device_error", "pa_strerror", "decode", "prefill", "prefill_split",
+    "append_kv",
 ]
 
 BF16 = 0
@@ -64,6 +66,12 @@ def lib():
         L.pa_append_kv.restype = I
         L.pa_prefill_paged.argtypes = [P, P, P, P, P, I, P, F] + [I] * 8 + [P]
         L.pa_prefill_paged.restype = I
+        L.pa_prefill_paged_split.argtypes = [P, P, P, P, P, I, P, F] + [I] * 9 + [P, Z, P]
+        L.pa_prefill_paged_split.restype = I
+        L.pa_prefill_partition_tokens.argtypes = [I] * 8
+        L.pa_prefill_partition_tokens.restype = I
+        L.pa_prefill_workspace_size.argtypes = [I] * 8
+        L.pa_prefill_workspace_size.restype = Z
         L.pa_decode_static_workspace.argtypes = [P, P, P, P, P, P, F] + [I] * 9 + [P]
         L.pa_decode_static_workspace.restype = I
         L.pa_last_device_error.argtypes = [P]
@@ -184,6 +192,33 @@ def pa_prefill_paged(q, k_cache, v_cache, block_table, ctx_lens, n_new, out, sca
     return _check(rc, "pa_prefill_paged")
 
 
+def pa_prefill_paged_split(q, k_cache, v_cache, block_table, ctx_lens, n_new, out,
+                           scale, n_q_heads, n_kv_heads, head_dim, page_size, batch,
+                           max_blocks_per_seq, num_pages, dtype, partition_tokens=0,
+                           workspace=None, workspace_bytes=0, stream=None) -> int:
+    rc = lib().pa_prefill_paged_split(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), n_new,
+        _ptr(out), float(scale), n_q_heads, n_kv_heads, head_dim, page_size, batch,
+        max_blocks_per_seq, num_pages, dtype, partition_tokens, _ptr(workspace),
+        workspace_bytes, _stream(stream))
+    return _check(rc, "pa_prefill_paged_split")
+
+
+def pa_prefill_partition_tokens(batch, n_new, n_q_heads, n_kv_heads, head_dim, page_size,
+                                max_blocks_per_seq, partition_tokens=0) -> int:
+    rc = lib().pa_prefill_partition_tokens(batch, n_new, n_q_heads, n_kv_heads, head_dim,
+                                           page_size, max_blocks_per_seq, partition_tokens)
+    if rc < 0:
+        raise PAError(rc, "pa_prefill_partition_tokens")
+    return rc
+
+
+def pa_prefill_workspace_size(batch, n_new, n_q_heads, n_kv_heads, head_dim, page_size,
+                              max_blocks_per_seq, partition_tokens=0) -> int:
+    return lib().pa_prefill_workspace_size(batch, n_new, n_q_heads, n_kv_heads, head_dim,
+                                           page_size, max_blocks_per_seq, partition_tokens)
+
+
 def pa_last_device_error(stream=None) -> int:
     """Synchronises the stream; returns and clears the device status word."""
     return lib().pa_last_device_error(_stream(stream))
@@ -229,4 +264,24 @@ def prefill(q, k_cache, v_cache, block_table, ctx_lens, scale, out=None, stream=
         out = torch.empty((B, n_new, hq, D), dtype=torch.float32, device=q.device)
     pa_prefill_paged(q, k_cache, v_cache, block_table, ctx_lens, n_new, out, scale,
                      hq, hkv, D, P, B, mb, pages, dtype_code(q), stream)
+    return out
+
+
+def prefill_split(q, k_cache, v_cache, block_table, ctx_lens, scale, partition_tokens=0,
+                  out=None, workspace=None, stream=None):
+    """pa_prefill_paged_split on tensors: q [B, n_new, h_q, D] (e.g. the gamma
+    drafted tokens of a speculative-decoding verify step); ctx_lens = cached
+    tokens before the chunk.  Returns fp32 [B, n_new, h_q, D]."""
+    import torch
+    B, n_new, hq, D = q.shape
+    pages, hkv, P, _ = k_cache.shape
+    mb = block_table.shape[1]
+    if out is None:
+        out = torch.empty((B, n_new, hq, D), dtype=torch.float32, device=q.device)
+    ws_bytes = pa_prefill_workspace_size(B, n_new, hq, hkv, D, P, mb, partition_tokens)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=q.device)
+    pa_prefill_paged_split(q, k_cache, v_cache, block_table, ctx_lens, n_new, out, scale,
+                           hq, hkv, D, P, B, mb, pages, dtype_code(q), partition_tokens,
+                           workspace, ws_bytes, stream)
     return out

@@ -207,6 +207,42 @@ int decode_plan(int batch, int n_q_heads, int n_kv_heads, int max_blocks,
   return PA_OK;
 }
 
+// Key-range partitions of the chunked prefill (multiples of 128 keys, the
+// kernel's key tile).  A CTA holds two row tiles of 128 (query, head) rows
+// and one CTA fits an SM; with fewer CTAs than SMs, a sequence's keys are cut
+// into as many ranges as keep the grid within two full waves (equal ranges
+// finish together, so a third, nearly empty wave would cost a whole range),
+// each range at least 512 keys.
+int prefill_plan(int batch, int n_new, int n_q_heads, int n_kv_heads, int max_blocks,
+                 int partition_tokens, int *part_tokens, int *n_parts) {
+  constexpr int kTile = 128;
+  if (partition_tokens < 0 || partition_tokens % kTile) return PA_ERR_PARTITION;
+  const int64_t max_tokens = static_cast<int64_t>(max_blocks) * kPageSize;
+  int64_t per = partition_tokens;
+  if (per == 0) {
+    const int gt = group_tile(n_q_heads / n_kv_heads);
+    const int64_t rows_per_cta = 2 * (128 / gt);  // queries of two row tiles
+    const int64_t items = static_cast<int64_t>(batch) * n_kv_heads *
+                          ((n_q_heads / n_kv_heads) / gt) *
+                          ((n_new + rows_per_cta - 1) / rows_per_cta);
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    if (items < sms) {
+      const int64_t want = (2 * sms) / items;
+      per = (max_tokens + want - 1) / want;
+      per = (per + kTile - 1) / kTile * kTile;
+      if (per < 4 * kTile) per = 4 * kTile;
+    }
+  }
+  if (per <= 0 || per >= max_tokens) {
+    *part_tokens = 0;
+    *n_parts = 1;
+  } else {
+    *part_tokens = static_cast<int>(per);
+    *n_parts = static_cast<int>((max_tokens + per - 1) / per);
+  }
+  return PA_OK;
+}
+
 }  // namespace
 }  // namespace pa
 
@@ -225,7 +261,9 @@ const char *pa_strerror(int status) {
     case PA_ERR_DTYPE: return "PA_ERR_DTYPE: dtype must be PA_BF16 or PA_F16";
     case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
     case PA_ERR_ALIGN: return "PA_ERR_ALIGN: pointer not 16-byte aligned";
-    case PA_ERR_PARTITION: return "PA_ERR_PARTITION: partition_tokens not a multiple of page_size";
+    case PA_ERR_PARTITION:
+      return "PA_ERR_PARTITION: partition_tokens not a multiple of page_size (decode) or 128 "
+             "(prefill)";
     case PA_ERR_CUDA: return "PA_ERR_CUDA: a CUDA call failed";
     case PA_ERR_BAD_BLOCK: return "PA_ERR_BAD_BLOCK: block-table entry outside the page pool";
     case PA_ERR_BAD_CTX: return "PA_ERR_BAD_CTX: context length outside [0, max_blocks*page_size]";
@@ -383,6 +421,83 @@ int pa_prefill_paged(const void *q, const void *k_cache, const void *v_cache,
   a.max_blocks = max_blocks_per_seq;
   a.num_pages = num_pages;
   a.bf16 = dtype == PA_BF16;
+  return launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_prefill_partition_tokens(int batch, int n_new, int n_q_heads, int n_kv_heads,
+                                int head_dim, int page_size, int max_blocks_per_seq,
+                                int partition_tokens) {
+  int rc = check_common(n_q_heads, n_kv_heads, head_dim, page_size, batch,
+                        max_blocks_per_seq, 1, PA_BF16);
+  if (rc) return rc;
+  if (n_new < 0 || n_new > (1 << 20)) return PA_ERR_SHAPE;
+  int pt = 0, np = 1;
+  rc = prefill_plan(batch, n_new, n_q_heads, n_kv_heads, max_blocks_per_seq,
+                    partition_tokens, &pt, &np);
+  return rc ? rc : pt;
+}
+
+size_t pa_prefill_workspace_size(int batch, int n_new, int n_q_heads, int n_kv_heads,
+                                 int head_dim, int page_size, int max_blocks_per_seq,
+                                 int partition_tokens) {
+  if (check_common(n_q_heads, n_kv_heads, head_dim, page_size, batch,
+                   max_blocks_per_seq, 1, PA_BF16))
+    return 0;
+  if (n_new <= 0 || n_new > (1 << 20)) return 0;
+  int pt = 0, np = 1;
+  if (prefill_plan(batch, n_new, n_q_heads, n_kv_heads, max_blocks_per_seq,
+                   partition_tokens, &pt, &np))
+    return 0;
+  if (np <= 1) return 0;
+  return prefill_partials_bytes(batch, n_new, n_q_heads, np, head_dim);
+}
+
+int pa_prefill_paged_split(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *ctx_lens,
+                           int n_new, float *out, float scale, int n_q_heads,
+                           int n_kv_heads, int head_dim, int page_size, int batch,
+                           int max_blocks_per_seq, int num_pages, pa_dtype dtype,
+                           int partition_tokens, void *workspace, size_t workspace_bytes,
+                           pa_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !out)
+    return PA_ERR_NULL;
+  int rc = check_common(n_q_heads, n_kv_heads, head_dim, page_size, batch,
+                        max_blocks_per_seq, num_pages, dtype);
+  if (rc) return rc;
+  if (n_new < 0 || n_new > (1 << 20)) return PA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_ALIGN;
+  int pt = 0, np = 1;
+  rc = prefill_plan(batch, n_new, n_q_heads, n_kv_heads, max_blocks_per_seq,
+                    partition_tokens, &pt, &np);
+  if (rc) return rc;
+  if (np > 1 && n_new > 0) {
+    const size_t need = prefill_partials_bytes(batch, n_new, n_q_heads, np, head_dim);
+    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_ALIGN;
+  }
+  if (n_new == 0) return PA_OK;
+  PrefillLaunch a;
+  rc = current_status_ptr(&a.status);
+  if (rc) return rc;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.ctx_lens = ctx_lens;
+  a.out = out;
+  a.scale = scale;
+  a.n_new = n_new;
+  a.n_q_heads = n_q_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.head_dim = head_dim;
+  a.batch = batch;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_pages = num_pages;
+  a.bf16 = dtype == PA_BF16;
+  a.n_parts = np;
+  a.part_tokens = pt;
+  a.workspace = np > 1 ? static_cast<float *>(workspace) : nullptr;
   return launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -639,7 +639,10 @@ __global__ void __launch_bounds__(NW * 32)
 // ---------------------------------------------------------------------------
 // Exact merge of partition states (the exponent law: M = max m_p,
 // l = sum e^(m_p - M) l_p, o = sum e^(m_p - M) O_p / l), one CTA of 128
-// threads per (sequence, head).  Thread (sl, qd) owns a float4 of head_dim
+// threads per row.  A row is (sequence b, query i < q_len, head h), stored at
+// (b q_len + i) n_q_heads + h; it saw T = ctx[b] keys (decode), or
+// ctx[b] + i + 1 (prefill: query i of a chunk that follows ctx[b] cached
+// tokens), so its partitions 0 .. ceil(T / part_tokens) - 1 hold states.  Thread (sl, qd) owns a float4 of head_dim
 // and every SL-th partition, and folds its partitions into a running
 // (m, l, O) with the same law as it reads them, so all its loads are
 // independent and a row costs about one memory round trip; the SL slices
@@ -648,24 +651,26 @@ template <int D>
 __global__ void __launch_bounds__(128)
     merge_kernel(const float *__restrict__ parts, const int32_t *__restrict__ ctx,
                  float *__restrict__ out, int *status, int n_q_heads, int n_parts,
-                 int part_tokens) {
+                 int part_tokens, int prefill) {
   constexpr int W = D + 4, Q = D / 4, SL = 128 / Q;
   __shared__ float2 sml[SL];
   __shared__ __align__(16) float sacc[SL][D];
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int h = blockIdx.x % n_q_heads, i = blockIdx.x / n_q_heads, b = blockIdx.y;
+  const int q_len = gridDim.x / n_q_heads, tid = threadIdx.x;
   griddep_release();
   griddep_wait();
   long T = ctx[b];
   if (T < 0) {
-    if (tid == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
+    if (tid == 0 && blockIdx.x == 0) record_error(status, PA_ERR_BAD_CTX);
     T = 0;
   }
+  if (prefill) T += i + 1;
   int n_valid = static_cast<int>((T + part_tokens - 1) / part_tokens);
   if (n_valid > n_parts) {
-    if (tid == 0 && h == 0) record_error(status, PA_ERR_BAD_CTX);
+    if (tid == 0 && blockIdx.x == 0) record_error(status, PA_ERR_BAD_CTX);
     n_valid = n_parts;
   }
-  const size_t row = static_cast<size_t>(b) * n_q_heads + h;
+  const size_t row = (static_cast<size_t>(b) * q_len + i) * n_q_heads + h;
   const float *base = parts + row * static_cast<size_t>(n_parts) * W;
 
   const int qd = tid % Q, sl = tid / Q;
@@ -764,7 +769,7 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
     const dim3 mgrid(a.n_q_heads, a.batch);
     if (launch_pdl(merge_kernel<D>, mgrid, dim3(128), 0, stream,
                    static_cast<const float *>(a.workspace), a.ctx_lens, a.out, a.status,
-                   a.n_q_heads, a.n_parts, a.part_pages * 16) != cudaSuccess)
+                   a.n_q_heads, a.n_parts, a.part_pages * 16, 0) != cudaSuccess)
       return PA_ERR_CUDA;
   }
   return PA_OK;
@@ -796,10 +801,23 @@ int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,
   const dim3 grid(n_q_heads, batch);
   if (head_dim == 128)
     merge_kernel<128><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                                n_q_heads, n_parts, partition_tokens);
+                                                n_q_heads, n_parts, partition_tokens, 0);
   else
     merge_kernel<64><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                               n_q_heads, n_parts, partition_tokens);
+                                               n_q_heads, n_parts, partition_tokens, 0);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int launch_merge_rows(const float *partials, const int32_t *ctx_lens, float *out, int *status,
+                      int batch, int n_q_heads, int head_dim, int n_parts,
+                      int partition_tokens, int n_new, cudaStream_t stream) {
+  const dim3 grid(n_q_heads * n_new, batch);
+  if (head_dim == 128)
+    merge_kernel<128><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
+                                                n_q_heads, n_parts, partition_tokens, 1);
+  else
+    merge_kernel<64><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
+                                               n_q_heads, n_parts, partition_tokens, 1);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -62,7 +62,24 @@ struct PrefillLaunch {
   float scale;
   int n_new, n_q_heads, n_kv_heads, head_dim, batch, max_blocks, num_pages;
   bool bf16;
+  // Key-range partitions (n_parts > 1): part_tokens keys each (a multiple of
+  // 128); partial states go to workspace, then a merge writes out.
+  int n_parts = 1, part_tokens = 0;
+  float *workspace = nullptr;
 };
+
+// Workspace of a split prefill: float [B][n_new][Hq][n_parts][D + 4].
+inline size_t prefill_partials_bytes(int batch, int n_new, int n_q_heads, int n_parts,
+                                     int head_dim) {
+  return static_cast<size_t>(batch) * n_new * n_q_heads * n_parts * (head_dim + 4) *
+         sizeof(float);
+}
+
+// Merge of prefill rows: row (b, i, h) of q_len = n_new queries saw
+// ctx_lens[b] + i + 1 keys.
+int launch_merge_rows(const float *partials, const int32_t *ctx_lens, float *out, int *status,
+                      int batch, int n_q_heads, int head_dim, int n_parts,
+                      int partition_tokens, int n_new, cudaStream_t stream);
 
 int launch_prefill(const PrefillLaunch &a, cudaStream_t stream);
 

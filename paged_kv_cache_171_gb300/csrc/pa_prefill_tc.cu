@@ -39,6 +39,7 @@ namespace pa {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kSlack = 8.0f;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRows = 128;       // rows per row tile (the MMA's M)
@@ -59,6 +60,12 @@ struct TcParams {
   float qscale;     // |scale| * log2 e, at least 1e-30
   uint32_t qsign;   // 0x80008000 when scale < 0 (folded into Q), else 0
   int n_new, n_q_heads, n_kv_heads, group, batch, max_blocks, num_pages;
+  // Key-range partitions: n_parts > 1 splits each sequence's keys into
+  // ranges of part_tiles key tiles; every CTA then writes its rows' partial
+  // states (O, m, l) to ws [batch][n_new][n_q_heads][n_parts][head_dim + 4]
+  // for the merge kernel instead of O / l to out.
+  float *ws;
+  int part_tiles, n_parts;
 };
 
 // Shared memory (offsets from a 1024-aligned base).  Operand tiles are
@@ -145,13 +152,15 @@ __device__ __forceinline__ void raise_abort(int *status, volatile int *abort_fla
   *abort_flag = 1;
 }
 
-// Per-CTA work description shared by all roles.
+// Per-CTA work description shared by all roles.  Key tiles are counted
+// from t0, the first tile of the CTA's key range (0 without partitions).
 struct TcWork {
   int b, g, hbase, q0;  // batch, kv head, first q head, first query of tile A
   int ctx;              // cached tokens of sequence b
+  int part, t0;         // key-range partition, its first key tile
   int nq[2];            // real queries in row tiles A and B (B may have none)
-  int n_tiles[2];       // key tiles each row tile visits (0: tile unused)
-  int kmax;             // last key any row of the CTA sees
+  int n_tiles[2];       // key tiles of the range each row tile visits (0: none)
+  int kmax;             // last key any row of the CTA sees (absolute)
   int n_kv_tiles;       // key tiles loaded = max(n_tiles)
 };
 
@@ -179,16 +188,17 @@ __device__ __forceinline__ void load_tiles(bool is_v, const CUtensorMap *map, ui
   };
   if (lane == 0) prefetch_tensormap(map);
   const int y_head = w.g * 16;
-  int wcur = load_window(0), wnext = load_window(1);
+  int wcur = load_window(w.t0 >> 2), wnext = load_window((w.t0 >> 2) + 1);
   const int n = w.n_kv_tiles;
   int issued = 0;
   bool ok = true;
-  for (int t = 0; t < n; ++t) {
-    if (t > 0 && (t & 3) == 0) {  // the tile starts a new 32-page window
+  for (int t = 0; t < n; ++t) {  // t counts the range's tiles; ta is absolute
+    const int ta = w.t0 + t;
+    if (t > 0 && (ta & 3) == 0) {  // the tile starts a new 32-page window
       wcur = wnext;
-      wnext = load_window((t >> 2) + 1);
+      wnext = load_window((ta >> 2) + 1);
     }
-    int idj = __shfl_sync(kFull, wcur, 8 * (t & 3) + (lane & 7));
+    int idj = __shfl_sync(kFull, wcur, 8 * (ta & 3) + (lane & 7));
     if (lane < 8 && static_cast<unsigned>(idj) >= static_cast<unsigned>(num_pages)) {
       record_error(status, PA_ERR_BAD_BLOCK);
       idj = 0;
@@ -211,9 +221,9 @@ __device__ __forceinline__ void load_tiles(bool is_v, const CUtensorMap *map, ui
     }
     ++issued;
   }
-  const int key0 = (n - 1) * kKeys;
+  const int key0 = (w.t0 + n - 1) * kKeys;
   const int first = w.kmax - key0 + 1;  // first row of the last V tile no row sees
-  if (is_v && ok && first < kKeys) {
+  if (is_v && ok && n > 0 && first < kKeys) {
     const int t = n - 1;
     if ((ok = warp_wait(bar(kBarV + t % S), (t / S) & 1, abort_flag))) {
       const uint32_t vst = ring + (t % S) * L::kKVBytes;
@@ -256,7 +266,7 @@ __device__ __forceinline__ void mma_tiles(int x, uint32_t sb, uint32_t tmem, con
   const uint64_t dv0 = tc::smem_desc_sw128(sb + L::kV0, L::kColBlk, 1024);
   const uint32_t tSx = tmem + x * kKeys, tOx = tmem + 2 * kKeys + x * D;
   const int n = w.n_kv_tiles, nx = w.n_tiles[x];
-  const int last_first = w.kmax - (n - 1) * kKeys + 1;
+  const int last_first = w.kmax - (w.t0 + n - 1) * kKeys + 1;
   const bool cleared = last_first < kKeys;  // the last V tile waits for the clearing
 
   auto s_mma = [&](int t) {  // S_x = Q_x K_t^T; then K stage t % SK is free for x
@@ -362,7 +372,7 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
     tc::wait_ld();
 
     // ---- mask, max of the raw scores, lazy move of the reference max
-    const int key0 = j * kKeys;
+    const int key0 = (w.t0 + j) * kKeys;
     if (key0 + kKeys - 1 > lim_all) {
       const int last = lim - key0;  // keys past this one are masked for row r
 #pragma unroll
@@ -436,11 +446,15 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
   }
   tc::fence_after_sync();
 
-  // ---- O / l for this row
+  // ---- O / l for this row, or the row's partial state for this key range
   const float l = l0 + l1;
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  float *dst = p.out +
-               ((static_cast<size_t>(w.b) * p.n_new + qx0 + qi) * p.n_q_heads + w.hbase + hh) * D;
+  const bool split = p.n_parts > 1;
+  const float inv = split ? 1.f : (l > 0.f ? 1.f / l : 0.f);
+  const size_t row =
+      (static_cast<size_t>(w.b) * p.n_new + qx0 + qi) * p.n_q_heads + w.hbase + hh;
+  float *dst = split ? p.ws + (row * p.n_parts + w.part) * (D + 4) : p.out + row * D;
+  if (split && qi < w.nq[x])
+    *reinterpret_cast<float2 *>(dst + D) = make_float2(m * kLn2, l);  // natural-log m
 #pragma unroll
   for (int cb = 0; cb < D / 32; ++cb) {
     uint32_t o[32];
@@ -475,7 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   w.b = blockIdx.z;
   w.g = blockIdx.y / n_sub;
   w.hbase = w.g * p.group + (blockIdx.y % n_sub) * GT;
-  w.q0 = blockIdx.x * 2 * BQ;
+  w.part = blockIdx.x % p.n_parts;
+  w.q0 = (blockIdx.x / p.n_parts) * 2 * BQ;
+  w.t0 = w.part * p.part_tiles;  // part_tiles = every tile when n_parts is 1
   int ctx = p.ctx_lens[w.b];
   const int maxT = p.max_blocks * 16;
   if (ctx < 0 || ctx + p.n_new > maxT) {
@@ -487,7 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int x = 0; x < 2; ++x) {
     w.nq[x] = max(0, min(BQ, p.n_new - (w.q0 + x * BQ)));
     const int kx = ctx + w.q0 + x * BQ + w.nq[x] - 1;  // last key a row of x sees
-    w.n_tiles[x] = w.nq[x] > 0 ? kx / kKeys + 1 : 0;
+    const int t_end = min(kx / kKeys + 1, w.t0 + p.part_tiles);
+    w.n_tiles[x] = w.nq[x] > 0 ? max(0, t_end - w.t0) : 0;
     if (w.nq[x] > 0) w.kmax = max(w.kmax, kx);
   }
   w.n_kv_tiles = max(w.n_tiles[0], w.n_tiles[1]);
@@ -587,10 +604,18 @@ int launch_tc_t(const PrefillLaunch &a, cudaStream_t stream) {
   p.batch = a.batch;
   p.max_blocks = a.max_blocks;
   p.num_pages = a.num_pages;
+  p.ws = a.workspace;
+  p.n_parts = a.n_parts > 1 ? a.n_parts : 1;
+  p.part_tiles = a.n_parts > 1 ? a.part_tokens / kKeys : (a.max_blocks * 16 + kKeys - 1) / kKeys;
   constexpr int BQ = kRows / GT;
-  const dim3 grid((a.n_new + 2 * BQ - 1) / (2 * BQ), a.n_kv_heads * (p.group / GT), a.batch);
+  const dim3 grid(((a.n_new + 2 * BQ - 1) / (2 * BQ)) * p.n_parts,
+                  a.n_kv_heads * (p.group / GT), a.batch);
   kern<<<grid, kThreads, L::kAlloc, stream>>>(kmap, vmap, p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (p.n_parts > 1)
+    return launch_merge_rows(a.workspace, a.ctx_lens, a.out, a.status, a.batch, a.n_q_heads,
+                             D, p.n_parts, a.part_tokens, a.n_new, stream);
+  return PA_OK;
 }
 
 template <int D, bool BF16>

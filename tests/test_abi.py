@@ -135,3 +135,45 @@ def test_product_package_does_not_reach_the_oracle():
                 text = open(os.path.join(root, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "pa_oracle" not in text and "liboracle" not in text, f
+
+
+def test_prefill_split_plan_and_workspace(L):
+    """Key-range partitions of the chunked prefill: multiples of 128 keys; the
+    workspace holds (O, m, l, 2 pad) per row and partition."""
+    for b, n_new, hq, hkv, d, mb, pt in [(4, 4, 64, 8, 128, 2048, 512),
+                                         (2, 70, 32, 8, 64, 300, 1024),
+                                         (1, 1, 16, 16, 128, 8, 128),
+                                         (3, 5, 8, 8, 128, 4, 128)]:
+        max_tokens = mb * 16
+        n_parts = -(-max_tokens // pt) if pt < max_tokens else 1
+        want = b * n_new * hq * n_parts * (d + 4) * 4 if n_parts > 1 else 0
+        assert L.pa_prefill_workspace_size(b, n_new, hq, hkv, d, 16, mb, pt) == want
+        got = L.pa_prefill_partition_tokens(b, n_new, hq, hkv, d, 16, mb, pt)
+        assert got == (pt if n_parts > 1 else 0)
+    assert L.pa_prefill_partition_tokens(4, 4, 64, 8, 128, 16, 2048, 100) == -9
+    assert L.pa_prefill_partition_tokens(4, 4, 64, 8, 128, 16, 2048, 48) == -9
+    # automatic: a multiple of 128 of at least 512 keys when row tiles are few,
+    # no split when they already fill the GPU
+    pt = L.pa_prefill_partition_tokens(4, 4, 64, 8, 128, 16, 2048, 0)
+    assert pt % 128 == 0 and pt >= 512 and pt < 2048 * 16
+    assert L.pa_prefill_partition_tokens(4, 512, 32, 8, 128, 16, 545, 0) == 0
+    assert L.pa_prefill_workspace_size(4, 512, 32, 8, 128, 16, 545, 0) == 0
+
+
+def test_prefill_split_rejects_bad_arguments(L):
+    P = FAKE
+    f = ctypes.c_float(0.1)
+    split = L.pa_prefill_paged_split
+    # missing or short workspace, before any launch
+    assert split(P, P, P, P, P, 4, P, f, 64, 8, 128, 16, 4, 2048, 16, 0, 512, None, 0,
+                 None) == -7
+    assert split(P, P, P, P, P, 4, P, f, 64, 8, 128, 16, 4, 2048, 16, 0, 512, P, 1024,
+                 None) == -7
+    assert split(P, P, P, P, P, 4, P, f, 64, 8, 128, 16, 4, 2048, 16, 0, 100, P, 1 << 30,
+                 None) == -9
+    assert split(None, P, P, P, P, 4, P, f, 64, 8, 128, 16, 4, 2048, 16, 0, 0, None, 0,
+                 None) == -1
+    assert split(P, P, P, P, P, 4, P, f, 64, 7, 128, 16, 4, 2048, 16, 0, 0, None, 0,
+                 None) == -2
+    assert split(P, P, P, P, P, 0, P, f, 64, 8, 128, 16, 4, 2048, 16, 0, 512, None, 0,
+                 None) == 0

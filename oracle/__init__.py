@@ -13,6 +13,9 @@ Functions and the passages they follow (page title, section):
                      19.6.2 (stable softmax), 19.7.3 (block table);
                      "吞吐与延迟的系统模型" 4-5 (GQA shares KV heads).
   decode_online   -- 19.6.2, the three-step online-softmax recurrence.
+  decode_window   -- decode over the attention-sink + sliding-window key set
+                     (ch. 19, KV-cache eviction: the first tokens and the most
+                     recent window are kept).
   partials/merge  -- 19.6.2's exponent law applied to chunk summaries.
   append_kv       -- "吞吐与延迟的系统模型" 4 (one new K and V row per step).
   prefill         -- 19.3.1 / 19.6.3, causal attention of a chunk of new
@@ -44,6 +47,7 @@ def _load():
         Dd = ctypes.c_double
         lib.oracle_decode.argtypes = [P, P, P, P, P, P, Dd] + [I] * 9
         lib.oracle_decode_online.argtypes = [P, P, P, P, P, P, Dd] + [I] * 8 + [P, I]
+        lib.oracle_decode_window.argtypes = [P, P, P, P, P, P, Dd] + [I] * 11
         lib.oracle_partials.argtypes = [P, P, P, P, P, P, Dd] + [I] * 11
         lib.oracle_merge.argtypes = [P, P, I, I, I]
         lib.oracle_append_kv.argtypes = [P, P, P, P, P, P, P] + [I] * 7
@@ -52,7 +56,8 @@ def _load():
         lib.oracle_decode_half.restype = Dd
         lib.oracle_max_threads.restype = I
         for f in ("oracle_decode", "oracle_decode_online", "oracle_partials",
-                  "oracle_merge", "oracle_append_kv", "oracle_prefill"):
+                  "oracle_merge", "oracle_append_kv", "oracle_prefill",
+                  "oracle_decode_window"):
             getattr(lib, f).restype = I
         _lib = lib
     return _lib
@@ -114,6 +119,25 @@ def decode(q, k_cache, v_cache, block_table, ctx_lens, scale, dtype,
                                n_threads)
     if rc:
         raise ValueError("oracle_decode: index out of range")
+    return out
+
+
+def decode_window(q, k_cache, v_cache, block_table, ctx_lens, scale, dtype, sink,
+                  window, n_threads: int = 0) -> np.ndarray:
+    """Decode attention over the attention-sink + sliding-window key set:
+    key t of a T-token sequence is kept iff t < sink or t >= T - window."""
+    q, kc, vc = bits(q), bits(k_cache), bits(v_cache)
+    bt, cl = _i32(block_table), _i32(ctx_lens)
+    batch, n_q_heads, head_dim = q.shape
+    num_pages, n_kv_heads, page_size, hd = _geom(kc)
+    assert hd == head_dim and vc.shape == kc.shape and bt.shape[0] == batch
+    out = np.zeros((batch, n_q_heads, head_dim), dtype=np.float64)
+    rc = _load().oracle_decode_window(_p(q), _p(kc), _p(vc), _p(bt), _p(cl), _p(out),
+                                      float(scale), n_q_heads, n_kv_heads, head_dim,
+                                      page_size, batch, bt.shape[1], num_pages, dtype,
+                                      int(sink), int(window), n_threads)
+    if rc:
+        raise ValueError("oracle_decode_window: index out of range")
     return out
 
 

@@ -190,6 +190,70 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache,
   return bad ? -1 : 0;
 }
 
+/* Decode attention over the attention-sink + sliding-window key set ("推理系统
+ * 与性能工程", KV-cache eviction: keep the first tokens of the sequence and a
+ * window of the most recent ones).  Key t of a T-token sequence is kept iff
+ * t < sink or t >= T - window; the softmax runs over the kept keys only (a
+ * row with none gives zeros).  out: double [batch, n_q_heads, head_dim]. */
+static int or_attend_kept(const or_cache *c, const double *qd, int b, int g, long T,
+                          long sink, long window, double scale, double *s,
+                          double *o) {
+  int D = c->head_dim;
+  for (int i = 0; i < D; ++i) o[i] = 0.0;
+  if (T == 0) return 0;
+  if (or_scores(c, qd, b, g, T, scale, s)) return -1;
+  double m = -INFINITY;
+  long kept = 0;
+  for (long t = 0; t < T; ++t)
+    if (t < sink || t >= T - window) {
+      if (s[t] > m) m = s[t];
+      ++kept;
+    }
+  if (kept == 0) return 0;
+  double denom = 0.0;
+  for (long t = 0; t < T; ++t) {
+    if (!(t < sink || t >= T - window)) continue;
+    double w = exp(s[t] - m);
+    denom += w;
+    const uint16_t *v = or_row(c, c->v_cache, b, g, t);
+    if (!v) return -1;
+    for (int i = 0; i < D; ++i) o[i] += w * or_dec(v[i], c->dtype);
+  }
+  for (int i = 0; i < D; ++i) o[i] /= denom;
+  return 0;
+}
+
+int oracle_decode_window(const uint16_t *q, const uint16_t *k_cache,
+                         const uint16_t *v_cache, const int32_t *block_table,
+                         const int32_t *ctx_lens, double *out, double scale,
+                         int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                         int batch, int max_blocks, int num_pages, int dtype, int sink,
+                         int window, int n_threads) {
+  if (or_check_heads(n_q_heads, n_kv_heads) || sink < 0 || window < 0) return -1;
+  for (int b = 0; b < batch; ++b)
+    if (ctx_lens[b] < 0 || (long)ctx_lens[b] > (long)max_blocks * page_size)
+      return -1;
+  or_cache c = {k_cache, v_cache, block_table, n_kv_heads, head_dim,
+                page_size, max_blocks, num_pages, dtype};
+  int G = n_q_heads / n_kv_heads;
+  int bad = 0;
+  or_set_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (long bh = 0; bh < (long)batch * n_q_heads; ++bh) {
+    int b = (int)(bh / n_q_heads), h = (int)(bh % n_q_heads), g = h / G;
+    long T = ctx_lens[b];
+    double *s = (double *)malloc(sizeof(double) * (T > 0 ? T : 1));
+    double *qd = (double *)malloc(sizeof(double) * head_dim);
+    const uint16_t *qr = q + ((size_t)b * n_q_heads + h) * head_dim;
+    for (int i = 0; i < head_dim; ++i) qd[i] = or_dec(qr[i], dtype);
+    if (or_attend_kept(&c, qd, b, g, T, sink, window, scale, s, out + bh * head_dim))
+      bad = 1;
+    free(s);
+    free(qd);
+  }
+  return bad ? -1 : 0;
+}
+
 /* The same result reached the way the pages' recurrence reaches it: the row
  * is cut into blocks at the given positions (cuts[] ascending, in tokens) and
  * the blocks are folded in order with

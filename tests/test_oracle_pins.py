@@ -323,3 +323,73 @@ def test_kv_byte_counts_match_the_pages():
     assert abs(b / 1e9 - gpt3["gb_approx"]) < 0.005
     # eq. 3 with S = B = 1 is the per-token figure of 19.4.2
     assert oracle.kv_bytes_eq3(32, 4096, 1, 1, 2) == oracle.kv_bytes_per_token(32, 4096, 2)
+
+
+# --- attention sink + sliding window (decode over a kept key set) ----------
+
+def _kept(T, sink, window):
+    return [t for t in range(T) if t < sink or t >= T - window]
+
+
+@pytest.mark.parametrize("sink,window", [(0, 64), (3, 40), (40, 0), (100, 100)])
+def test_window_covering_the_sequence_equals_plain_decode(sink, window):
+    """Keeping every key is plain decode (catches a window that drops the
+    last key or a sink that drops the first)."""
+    g, q, kc, vc = _rand_paged(21, lens=(23, 40))
+    k_cache, v_cache, bt = scatter_to_pages(kc, vc, [23, 40], 4, g)
+    lens = np.array([23, 40], np.int32)
+    full = oracle.decode(q, k_cache, v_cache, bt, lens, 0.3, oracle.BF16)
+    # every key of both sequences is kept: sink + window >= T
+    keep_all = all(len(_kept(int(T), sink, window)) == int(T) for T in lens)
+    got = oracle.decode_window(q, k_cache, v_cache, bt, lens, 0.3, oracle.BF16, sink, window)
+    if keep_all:
+        np.testing.assert_allclose(got, full, rtol=0, atol=1e-14)
+    else:
+        assert not np.allclose(got, full)
+
+
+def test_window_of_one_returns_the_last_v_and_sink_of_one_the_first():
+    """Catches an off-by-one at either end of the kept set."""
+    g, q, kc, vc = _rand_paged(22, lens=(9, 17))
+    k_cache, v_cache, bt = scatter_to_pages(kc, vc, [9, 17], 4, g)
+    lens = np.array([9, 17], np.int32)
+    last = oracle.decode_window(q, k_cache, v_cache, bt, lens, 0.3, oracle.BF16, 0, 1)
+    first = oracle.decode_window(q, k_cache, v_cache, bt, lens, 0.3, oracle.BF16, 1, 0)
+    none = oracle.decode_window(q, k_cache, v_cache, bt, lens, 0.3, oracle.BF16, 0, 0)
+    for b, T in enumerate(lens):
+        for h in range(4):
+            assert np.array_equal(last[b, h], vc[b, h // 2, T - 1].double().numpy())
+            assert np.array_equal(first[b, h], vc[b, h // 2, 0].double().numpy())
+    assert np.array_equal(none, np.zeros_like(none))
+
+
+@pytest.mark.parametrize("sink,window", [(4, 16), (1, 5), (7, 33), (0, 20), (13, 0)])
+def test_window_matches_sdpa_on_the_gathered_keys(sink, window):
+    """Library route: torch SDPA (float64) on the kept keys gathered in order
+    (catches mixing up the two ranges or a wrong sequence end)."""
+    lens = [57, 70]
+    g, q, kc, vc = _rand_paged(23, lens=tuple(lens))
+    k_cache, v_cache, bt = scatter_to_pages(kc, vc, lens, 4, g)
+    got = oracle.decode_window(q, k_cache, v_cache, bt, np.array(lens, np.int32), 0.25,
+                               oracle.BF16, sink, window)
+    for b, T in enumerate(lens):
+        idx = torch.tensor(_kept(T, sink, window), dtype=torch.int64)
+        kb = kc[b:b + 1].index_select(2, idx)
+        vb = vc[b:b + 1].index_select(2, idx)
+        ref = sdpa_reference(q[b:b + 1], kb, vb, [len(idx)], 0.25)
+        np.testing.assert_allclose(got[b:b + 1], ref, rtol=0, atol=1e-12)
+
+
+def test_window_hand_derived_case():
+    """T = 3, sink 1, window 1: keys 0 and 2 only; key 1 would dominate if it
+    were kept.  q = (1, 0), k = (0, 0), (8, 0), (1, 0), v = e1, (5, 5), e2:
+    weights 1 / (1 + e) and e / (1 + e)."""
+    kc = torch.tensor([[[[0., 0.], [8., 0.], [1., 0.]]]], dtype=torch.bfloat16)
+    vc = torch.tensor([[[[1., 0.], [5., 5.], [0., 1.]]]], dtype=torch.bfloat16)
+    q = torch.tensor([[[1., 0.]]], dtype=torch.bfloat16)
+    g = torch.Generator().manual_seed(0)
+    k_cache, v_cache, bt = scatter_to_pages(kc, vc, [3], 2, g)
+    got = oracle.decode_window(q, k_cache, v_cache, bt, np.array([3], np.int32), 1.0,
+                               oracle.BF16, 1, 1)
+    e = math.e
+    np.testing.assert_allclose(got[0, 0], [1 / (1 + e), e / (1 + e)], rtol=0, atol=1e-15)

@@ -457,6 +457,52 @@ def run_verify(torch, pa, workloads, steps, warmup, peaks, gamma=4):
     return res
 
 
+def run_window(torch, pa, workloads, steps, warmup, peaks, sink=4, window=4096):
+    """Attention-sink + sliding-window decode (pa_decode_window): 32 sequences
+    x 32768 cached tokens, 64/8 heads, bf16, 4 sink tokens and a 4096-token
+    window.  Algorithmic bytes = K/V of the sink + window keys + q + fp32
+    out; plain decode of the same caches is timed beside it."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, hq, hkv, D, ctx = 32, 64, 8, 128, 32768
+    case = workloads.paged_case(layers=1, batch=B, n_q_heads=hq, n_kv_heads=hkv,
+                                head_dim=D, page_size=16, ctx=[ctx] * B, dtype="bf16",
+                                seed=1007, device=dev)
+    mb = case.block_table.shape[2]
+    out = torch.empty((B, hq, D), dtype=torch.float32, device=dev)
+    ws_bytes = pa.pa_decode_window_workspace_size(B, hq, hkv, D, 16, mb, sink, window, 0)
+    ws = torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    kept = min(ctx, sink + window)
+    nbytes = B * (2 * kept * hkv * D * 2 + hq * D * (2 + 4))
+
+    def time_it(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    ms = time_it(lambda: pa.pa_decode_window(
+        case.q[0], case.k_cache, case.v_cache, case.block_table[0], case.ctx_lens, out,
+        case.scale, hq, hkv, D, 16, B, mb, case.k_cache.shape[0], case.dtype_code, sink,
+        window, 0, ws, ws_bytes, stream.cuda_stream))
+    assert pa.pa_last_device_error() == 0
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res = {"ms_per_step": round(ms, 4), "GB_s": round(gbs, 1),
+           "frac_of_hbm_peak": round(gbs / peaks.get("hbm_gbs", 6800.0), 4),
+           "sink": sink, "window": window, "context": ctx, "bytes_per_step": nbytes,
+           "kernel": "decode_kernel over the sink + window pages (+ merge when split)",
+           "l2": "inputs larger than 2x L2, no flush; steps timed back to back"}
+    del case, out, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_baseline_sample(torch, case, cfg, layers_budget_s=10.0):
     """The float64 oracle, as it stands, on whole layers of the headline
     workload until ~budget seconds pass (at least one layer)."""
@@ -571,6 +617,7 @@ def main_ours(args):
                                                   "mha_b1_ctx512", 20, 5)
         other["prefill_b4_512over8192"] = run_prefill(torch, pa, workloads, 10, 3, peaks)
         other["verify_gamma4_b4_ctx32k"] = run_verify(torch, pa, workloads, 20, 3, peaks)
+        other["window_sink4_w4096_b32_ctx32k"] = run_window(torch, pa, workloads, 20, 3, peaks)
         for k, v in other.items():
             if "GB_s" in v:
                 v["frac_of_hbm_peak"] = round(v["GB_s"] / hbm, 4)

@@ -111,6 +111,36 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
               pa_dtype dtype, int partition_tokens, void *workspace,
               size_t workspace_bytes, pa_stream_t stream);
 
+/*
+ * pa_decode_window -- decode attention over an attention sink plus a sliding
+ * window of recent keys (ch. 19 "推理系统与性能工程", KV-cache eviction: keep
+ * the first tokens and the most recent window).
+ *
+ * Same arguments and result layout as pa_decode, plus sink_tokens and
+ * window_tokens (both >= 0, PA_ERR_SHAPE otherwise).  Key t of a sequence of
+ * T = ctx_lens[b] tokens is attended iff t < sink_tokens or
+ * t >= T - window_tokens; when sink_tokens + window_tokens >= T every key is
+ * (plain decode), and a row with no attended key gives zeros.  Only the
+ * attended keys' pages are read, so the HBM traffic is that of
+ * sink + window tokens whatever T is.  Partitions (partition_tokens, as in
+ * pa_decode) cut the attended keys; the workspace is sized by
+ * pa_decode_window_workspace_size.  The block table still maps every
+ * position below T (the pages in the gap are simply not read).
+ */
+int pa_decode_window(const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, const int32_t *ctx_lens, float *out,
+                     float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                     int page_size, int batch, int max_blocks_per_seq, int num_pages,
+                     pa_dtype dtype, int sink_tokens, int window_tokens,
+                     int partition_tokens, void *workspace, size_t workspace_bytes,
+                     pa_stream_t stream);
+
+/* Workspace bytes pa_decode_window needs (0 when it runs in a single pass). */
+size_t pa_decode_window_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                       int head_dim, int page_size, int max_blocks_per_seq,
+                                       int sink_tokens, int window_tokens,
+                                       int partition_tokens);
+
 /* The partition size pa_decode would use (0 = a single pass, no workspace)
  * for these arguments and partition_tokens (0 = automatic), on the current
  * device.  Returns a negative PA_ERR_* on invalid arguments. */

@@ -22,6 +22,7 @@ __all__ = [
     "pa_decode_static_workspace",
     "pa_merge_partials", "pa_append_kv", "pa_prefill_paged",
     "pa_prefill_paged_split", "pa_prefill_partition_tokens", "pa_prefill_workspace_size",
+    "pa_decode_window", "pa_decode_window_workspace_size", "decode_window",
     "pa_last_device_error", "pa_strerror", "decode", "prefill", "prefill_split",
     "append_kv",
 ]
@@ -72,6 +73,10 @@ def lib():
         L.pa_prefill_partition_tokens.restype = I
         L.pa_prefill_workspace_size.argtypes = [I] * 8
         L.pa_prefill_workspace_size.restype = Z
+        L.pa_decode_window.argtypes = [P, P, P, P, P, P, F] + [I] * 11 + [P, Z, P]
+        L.pa_decode_window.restype = I
+        L.pa_decode_window_workspace_size.argtypes = [I] * 9
+        L.pa_decode_window_workspace_size.restype = Z
         L.pa_decode_static_workspace.argtypes = [P, P, P, P, P, P, F] + [I] * 9 + [P]
         L.pa_decode_static_workspace.restype = I
         L.pa_last_device_error.argtypes = [P]
@@ -219,6 +224,26 @@ def pa_prefill_workspace_size(batch, n_new, n_q_heads, n_kv_heads, head_dim, pag
                                            page_size, max_blocks_per_seq, partition_tokens)
 
 
+def pa_decode_window(q, k_cache, v_cache, block_table, ctx_lens, out, scale, n_q_heads,
+                     n_kv_heads, head_dim, page_size, batch, max_blocks_per_seq, num_pages,
+                     dtype, sink_tokens, window_tokens, partition_tokens=0, workspace=None,
+                     workspace_bytes=0, stream=None) -> int:
+    rc = lib().pa_decode_window(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), _ptr(out),
+        float(scale), n_q_heads, n_kv_heads, head_dim, page_size, batch, max_blocks_per_seq,
+        num_pages, dtype, sink_tokens, window_tokens, partition_tokens, _ptr(workspace),
+        workspace_bytes, _stream(stream))
+    return _check(rc, "pa_decode_window")
+
+
+def pa_decode_window_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, page_size,
+                                    max_blocks_per_seq, sink_tokens, window_tokens,
+                                    partition_tokens=0) -> int:
+    return lib().pa_decode_window_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+                                                 page_size, max_blocks_per_seq, sink_tokens,
+                                                 window_tokens, partition_tokens)
+
+
 def pa_last_device_error(stream=None) -> int:
     """Synchronises the stream; returns and clears the device status word."""
     return lib().pa_last_device_error(_stream(stream))
@@ -284,4 +309,24 @@ def prefill_split(q, k_cache, v_cache, block_table, ctx_lens, scale, partition_t
     pa_prefill_paged_split(q, k_cache, v_cache, block_table, ctx_lens, n_new, out, scale,
                            hq, hkv, D, P, B, mb, pages, dtype_code(q), partition_tokens,
                            workspace, ws_bytes, stream)
+    return out
+
+
+def decode_window(q, k_cache, v_cache, block_table, ctx_lens, scale, sink_tokens,
+                  window_tokens, partition_tokens=0, out=None, workspace=None, stream=None):
+    """pa_decode_window on tensors (shapes as decode()): attends keys t < sink_tokens
+    and t >= T - window_tokens of each sequence.  Returns fp32 [B, h_q, D]."""
+    import torch
+    B, hq, D = q.shape
+    pages, hkv, P, _ = k_cache.shape
+    mb = block_table.shape[1]
+    if out is None:
+        out = torch.empty((B, hq, D), dtype=torch.float32, device=q.device)
+    ws_bytes = pa_decode_window_workspace_size(B, hq, hkv, D, P, mb, sink_tokens,
+                                               window_tokens, partition_tokens)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=q.device)
+    pa_decode_window(q, k_cache, v_cache, block_table, ctx_lens, out, scale, hq, hkv, D, P,
+                     B, mb, pages, dtype_code(q), sink_tokens, window_tokens,
+                     partition_tokens, workspace, ws_bytes, stream)
     return out

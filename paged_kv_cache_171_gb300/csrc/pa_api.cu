@@ -301,12 +301,25 @@ size_t pa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
   return decode_partials_bytes(batch, n_q_heads, np, head_dim);
 }
 
-int pa_decode(const void *q, const void *k_cache, const void *v_cache,
-              const int32_t *block_table, const int32_t *ctx_lens, float *out,
-              float scale, int n_q_heads, int n_kv_heads, int head_dim,
-              int page_size, int batch, int max_blocks_per_seq, int num_pages,
-              pa_dtype dtype, int partition_tokens, void *workspace,
-              size_t workspace_bytes, pa_stream_t stream) {
+}  // extern "C"
+
+namespace pa {
+namespace {
+// Pages a sequence's query may attend: every table entry, or with an
+// attention sink and a window at most ceil(sink/16) + ceil(window/16) + 1.
+int attended_blocks(int max_blocks, int sink, int window) {
+  if (window < 0) return max_blocks;
+  const int64_t n = (static_cast<int64_t>(sink) + 15) / 16 +
+                    (static_cast<int64_t>(window) + 15) / 16 + 1;
+  return static_cast<int>(n < max_blocks ? n : max_blocks);
+}
+
+int decode_impl(const void *q, const void *k_cache, const void *v_cache,
+                const int32_t *block_table, const int32_t *ctx_lens, float *out,
+                float scale, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                int batch, int max_blocks_per_seq, int num_pages, pa_dtype dtype,
+                int sink, int window, int partition_tokens, void *workspace,
+                size_t workspace_bytes, pa_stream_t stream) {
   if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !out)
     return PA_ERR_NULL;
   int rc = check_common(n_q_heads, n_kv_heads, head_dim, page_size, batch,
@@ -315,7 +328,7 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_ALIGN;
   int pp = 0, np = 1, wp = 0;
-  rc = decode_plan(batch, n_q_heads, n_kv_heads, max_blocks_per_seq,
+  rc = decode_plan(batch, n_q_heads, n_kv_heads, attended_blocks(max_blocks_per_seq, sink, window),
                    partition_tokens, &pp, &np, &wp);
   if (rc) return rc;
   if (np > 1) {
@@ -344,7 +357,48 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
   a.part_pages = pp;
   a.n_parts = np;
   a.warp_parts = wp;
+  a.sink = sink;
+  a.window = window;
   return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+}  // namespace
+}  // namespace pa
+
+extern "C" {
+
+int pa_decode(const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_table, const int32_t *ctx_lens, float *out,
+              float scale, int n_q_heads, int n_kv_heads, int head_dim,
+              int page_size, int batch, int max_blocks_per_seq, int num_pages,
+              pa_dtype dtype, int partition_tokens, void *workspace,
+              size_t workspace_bytes, pa_stream_t stream) {
+  return decode_impl(q, k_cache, v_cache, block_table, ctx_lens, out, scale, n_q_heads,
+                     n_kv_heads, head_dim, page_size, batch, max_blocks_per_seq, num_pages,
+                     dtype, 0, -1, partition_tokens, workspace, workspace_bytes, stream);
+}
+
+int pa_decode_window(const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, const int32_t *ctx_lens, float *out,
+                     float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                     int page_size, int batch, int max_blocks_per_seq, int num_pages,
+                     pa_dtype dtype, int sink_tokens, int window_tokens,
+                     int partition_tokens, void *workspace, size_t workspace_bytes,
+                     pa_stream_t stream) {
+  if (sink_tokens < 0 || window_tokens < 0) return PA_ERR_SHAPE;
+  return decode_impl(q, k_cache, v_cache, block_table, ctx_lens, out, scale, n_q_heads,
+                     n_kv_heads, head_dim, page_size, batch, max_blocks_per_seq, num_pages,
+                     dtype, sink_tokens, window_tokens, partition_tokens, workspace,
+                     workspace_bytes, stream);
+}
+
+size_t pa_decode_window_workspace_size(int batch, int n_q_heads, int n_kv_heads,
+                                       int head_dim, int page_size, int max_blocks_per_seq,
+                                       int sink_tokens, int window_tokens,
+                                       int partition_tokens) {
+  if (sink_tokens < 0 || window_tokens < 0) return 0;
+  return pa_decode_workspace_size(
+      batch, n_q_heads, n_kv_heads, head_dim, page_size,
+      attended_blocks(max_blocks_per_seq, sink_tokens, window_tokens), partition_tokens);
 }
 
 int pa_merge_partials(const float *partials, const int32_t *ctx_lens,

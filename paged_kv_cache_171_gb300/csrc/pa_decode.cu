@@ -60,6 +60,45 @@ struct DecodeParams {
   int n_q_heads, n_kv_heads, group, batch, max_blocks, num_pages;
   int part_pages, n_parts;
   int warp_parts;  // > 0: each warp owns this many whole partitions
+  int sink, window;  // window >= 0: only the first `sink` and the last
+                     // `window` keys of each sequence are attended
+};
+
+// The keys a sequence's query attends, as a list of virtual pages.  Without
+// a window every page 0 .. ceil(T/16) - 1 in order.  With an attention sink
+// of S keys and a window of W keys (S + W < T): the sink pages
+// 0 .. ceil(S/16) - 1, then the window pages floor((T-W)/16) .. ceil(T/16) - 1;
+// a page holding both the sink's end and the window's start appears twice,
+// each time with its own key range.  Virtual page v covers keys
+// [16 lp + lo, 16 lp + hi) of logical page lp.
+struct KeySet {
+  int T, n_s, s_end, wf, w_lo, n_v;
+  __device__ void init(int T_, int sink, int window) {
+    T = T_;
+    if (window < 0 || sink + window >= T) {  // every key
+      n_s = n_v = (T + 15) >> 4;
+      s_end = T;
+      wf = 0;
+      w_lo = T;
+    } else {
+      s_end = sink;
+      n_s = (sink + 15) >> 4;
+      w_lo = T - window;
+      wf = w_lo >> 4;
+      n_v = n_s + (window > 0 ? ((T + 15) >> 4) - wf : 0);
+    }
+  }
+  __device__ int logical(int v) const { return v < n_s ? v : wf + (v - n_s); }
+  __device__ void range(int v, int &lo, int &hi) const {
+    if (v < n_s) {
+      lo = 0;
+      hi = min(16, s_end - 16 * v);
+    } else {
+      const int lp = wf + (v - n_s);
+      lo = max(0, w_lo - 16 * lp);
+      hi = min(16, T - 16 * lp);
+    }
+  }
 };
 
 // Shared-memory plan of one CTA.
@@ -104,10 +143,13 @@ struct PageRing {
   int *status;
   int first, stride, n_i, num_pages, y_page, y_head;
   int ids_cur, ids_nxt;
+  KeySet ks;  // chunk i is virtual page first + stride * i of this key set
 
   // The raw table entry; checked only when it is used, so the load's latency
   // is hidden behind the 32 chunks that come first.
-  __device__ int fetch_id(int i) { return i < n_i ? __ldg(bt_row + first + stride * i) : 0; }
+  __device__ int fetch_id(int i) {
+    return i < n_i ? __ldg(bt_row + ks.logical(first + stride * i)) : 0;
+  }
   // Lane j holds the page of chunk 32k + j; the next 32 are fetched early.
   __device__ void start(int lane) {
     ids_cur = fetch_id(lane);
@@ -176,7 +218,8 @@ __device__ __forceinline__ bool pages_cuda_core(Ring &ring, int i_begin, int i_e
   for (int i = i_begin; i < i_end; ++i) {
     if (!ring.wait(i, lane)) { ok = false; break; }
     const uint32_t st = ring.stage(i);
-    const int valid = min(16, T - ring.page(i) * 16);
+    int lo, valid;  // keys [lo, valid) of the page are attended
+    ring.ks.range(ring.page(i), lo, valid);
 
     float sc[GT];
     {
@@ -205,7 +248,7 @@ __device__ __forceinline__ bool pages_cuda_core(Ring &ring, int i_begin, int i_e
       for (int h = 0; h < GT; ++h) {
         float v = acc[h].x + acc[h].y;
         v += __shfl_xor_sync(kFull, v, 16);
-        sc[h] = (tok < valid) ? v : -INFINITY;
+        sc[h] = (tok >= lo && tok < valid) ? v : -INFINITY;
       }
     }
 
@@ -256,7 +299,7 @@ __device__ __forceinline__ bool pages_cuda_core(Ring &ring, int i_begin, int i_e
           O2[h][0] = __ffma2_rn(make_float2(pw[h], pw[h]), v01, O2[h][0]);
       }
     };
-    if (valid == 16) {
+    if (lo == 0 && valid == 16) {
 #pragma unroll
       for (int t4 = 0; t4 < 16; t4 += 4) {
         float4 pp[GT];
@@ -273,8 +316,8 @@ __device__ __forceinline__ bool pages_cuda_core(Ring &ring, int i_begin, int i_e
         }
       }
     } else {
-      // V rows past the sequence end are never read.
-      for (int t = 0; t < valid; ++t) {
+      // V rows outside the attended keys are never read.
+      for (int t = lo; t < valid; ++t) {
         float pw[GT];
 #pragma unroll
         for (int h = 0; h < GT; ++h) pw[h] = p_s[h * 16 + t];
@@ -330,10 +373,12 @@ __device__ __forceinline__ bool pages_mma(Ring &ring, int i_begin, int i_end,
   for (int i = i_begin; i < i_end; ++i) {
     if (!ring.wait(i, lane)) { ok = false; break; }
     const uint32_t st = ring.stage(i);
-    const int valid = min(16, T - ring.page(i) * 16);
+    int lo, valid;  // keys [lo, valid) of the page are attended
+    ring.ks.range(ring.page(i), lo, valid);
     if (valid < 16) {
-      // V rows past the sequence end may hold non-finite junk, and 0 * inf is
-      // NaN inside the MMA: clear them (the next TMA overwrites the stage).
+      // V rows past the attended keys may hold non-finite junk (past the
+      // sequence end), and 0 * inf is NaN inside the MMA: clear them in the
+      // stage (the next TMA overwrites it).
       const int n = (16 - valid) * (D / 8);
       for (int e = lane; e < n; e += 32) {
         const int r = valid + e / (D / 8), c = e % (D / 8);
@@ -359,7 +404,8 @@ __device__ __forceinline__ bool pages_mma(Ring &ring, int i_begin, int i_end,
                   sacc[1][1] * qscale};
     const int keys[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) s[j] = (real && keys[j] < valid) ? s[j] : -INFINITY;
+    for (int j = 0; j < 4; ++j)
+      s[j] = (real && keys[j] >= lo && keys[j] < valid) ? s[j] : -INFINITY;
     const float tmax = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
     if (__any_sync(kFull, tmax > m_r + kRescaleSlack)) {
       float mt = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
@@ -430,7 +476,9 @@ __global__ void __launch_bounds__(NW * 32)
     if (tid == 0) record_error(p.status, PA_ERR_BAD_CTX);
     T = T < 0 ? 0 : maxT;
   }
-  const int n_pages = (T + 15) >> 4;
+  KeySet ks;
+  ks.init(T, p.sink, p.window);
+  const int n_pages = ks.n_v;  // virtual pages of the attended keys
   int pg0 = 0, pg1 = n_pages;  // this CTA's pages
   if (ppw > 0) {
     pg0 = blockIdx.x * NW * ppw * p.part_pages;
@@ -472,6 +520,7 @@ __global__ void __launch_bounds__(NW * 32)
     ring.n_i = ring.first < pg1 ? (pg1 - ring.first + NW - 1) / NW : 0;
   }
   ring.num_pages = p.num_pages;
+  ring.ks = ks;
   ring.y_page = p.n_kv_heads * 16;
   ring.y_head = g * 16;
   ring.start(lane);
@@ -651,7 +700,7 @@ template <int D>
 __global__ void __launch_bounds__(128)
     merge_kernel(const float *__restrict__ parts, const int32_t *__restrict__ ctx,
                  float *__restrict__ out, int *status, int n_q_heads, int n_parts,
-                 int part_tokens, int prefill) {
+                 int part_tokens, int prefill, int sink, int window) {
   constexpr int W = D + 4, Q = D / 4, SL = 128 / Q;
   __shared__ float2 sml[SL];
   __shared__ __align__(16) float sacc[SL][D];
@@ -665,7 +714,11 @@ __global__ void __launch_bounds__(128)
     T = 0;
   }
   if (prefill) T += i + 1;
-  int n_valid = static_cast<int>((T + part_tokens - 1) / part_tokens);
+  // partitions cut the attended keys' virtual pages (all pages without a window)
+  long span = T;
+  if (window >= 0 && sink + window < T)
+    span = 16L * (((sink + 15) >> 4) + (window > 0 ? ((T + 15) >> 4) - ((T - window) >> 4) : 0));
+  int n_valid = static_cast<int>((span + part_tokens - 1) / part_tokens);
   if (n_valid > n_parts) {
     if (tid == 0 && blockIdx.x == 0) record_error(status, PA_ERR_BAD_CTX);
     n_valid = n_parts;
@@ -760,6 +813,8 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   p.part_pages = a.part_pages;
   p.n_parts = a.n_parts;
   p.warp_parts = a.warp_parts;
+  p.sink = a.sink;
+  p.window = a.window;
   const int gx = a.warp_parts > 0 ? (a.n_parts + NW * a.warp_parts - 1) / (NW * a.warp_parts)
                                   : a.n_parts;
   const dim3 grid(gx, a.n_kv_heads * (p.group / GT), a.batch);
@@ -769,7 +824,8 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
     const dim3 mgrid(a.n_q_heads, a.batch);
     if (launch_pdl(merge_kernel<D>, mgrid, dim3(128), 0, stream,
                    static_cast<const float *>(a.workspace), a.ctx_lens, a.out, a.status,
-                   a.n_q_heads, a.n_parts, a.part_pages * 16, 0) != cudaSuccess)
+                   a.n_q_heads, a.n_parts, a.part_pages * 16, 0, a.sink, a.window) !=
+        cudaSuccess)
       return PA_ERR_CUDA;
   }
   return PA_OK;
@@ -801,10 +857,12 @@ int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,
   const dim3 grid(n_q_heads, batch);
   if (head_dim == 128)
     merge_kernel<128><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                                n_q_heads, n_parts, partition_tokens, 0);
+                                                n_q_heads, n_parts, partition_tokens, 0, 0,
+                                                -1);
   else
     merge_kernel<64><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                               n_q_heads, n_parts, partition_tokens, 0);
+                                               n_q_heads, n_parts, partition_tokens, 0, 0,
+                                               -1);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -814,10 +872,12 @@ int launch_merge_rows(const float *partials, const int32_t *ctx_lens, float *out
   const dim3 grid(n_q_heads * n_new, batch);
   if (head_dim == 128)
     merge_kernel<128><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                                n_q_heads, n_parts, partition_tokens, 1);
+                                                n_q_heads, n_parts, partition_tokens, 1, 0,
+                                                -1);
   else
     merge_kernel<64><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                               n_q_heads, n_parts, partition_tokens, 1);
+                                               n_q_heads, n_parts, partition_tokens, 1, 0,
+                                               -1);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

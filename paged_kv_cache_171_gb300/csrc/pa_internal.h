@@ -29,6 +29,10 @@ struct DecodeLaunch {
   int part_pages;  // pages per partition; 0 = a single pass over the sequence
   int n_parts;     // partitions per sequence (1 for a single pass)
   int warp_parts;  // > 0: each warp owns this many whole partitions
+  // Attention sink + sliding window: window >= 0 attends only keys t < sink
+  // and t >= T - window (window < 0: every key).  Partitions then cut the
+  // attended keys' pages.
+  int sink = 0, window = -1;
 };
 
 constexpr int kDecodeWarps = 4;  // warps per decode CTA

@@ -177,3 +177,23 @@ def test_prefill_split_rejects_bad_arguments(L):
                  None) == -2
     assert split(P, P, P, P, P, 0, P, f, 64, 8, 128, 16, 4, 2048, 16, 0, 512, None, 0,
                  None) == 0
+
+
+def test_decode_window_arguments_and_workspace(L):
+    P = FAKE
+    f = ctypes.c_float(0.1)
+    win = L.pa_decode_window
+    assert win(P, P, P, P, P, P, f, 32, 8, 128, 16, 2, 64, 16, 0, -1, 8, 0, None, 0,
+               None) == -5
+    assert win(P, P, P, P, P, P, f, 32, 8, 128, 16, 2, 64, 16, 0, 4, -2, 0, None, 0,
+               None) == -5
+    assert win(None, P, P, P, P, P, f, 32, 8, 128, 16, 2, 64, 16, 0, 4, 8, 0, None, 0,
+               None) == -1
+    # partitions cut the attended pages: at most ceil(s/16) + ceil(w/16) + 1
+    mb = 2048
+    for sink, window, pt in [(4, 4096, 512), (0, 100, 16), (16, 0, 16), (40000, 40000, 512)]:
+        att = min(mb, -(-sink // 16) + -(-window // 16) + 1)
+        n_parts = -(-att * 16 // pt) if pt < att * 16 else 1
+        want = _ws_bytes(4, 64, 8, 128, n_parts) if n_parts > 1 else 0
+        assert L.pa_decode_window_workspace_size(4, 64, 8, 128, 16, mb, sink, window, pt) == want
+    assert L.pa_decode_window_workspace_size(4, 64, 8, 128, 16, mb, -1, 8, 0) == 0

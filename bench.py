@@ -503,6 +503,91 @@ def run_window(torch, pa, workloads, steps, warmup, peaks, sink=4, window=4096):
     return res
 
 
+def run_prefix_sharing(torch, pa, steps, warmup, peaks, B=32, prefix=8192, suffix=128):
+    """Prefix sharing through the page pool: B sequences forked from one
+    prefix of `prefix` tokens, each with `suffix` tokens of its own (32/8
+    heads, D 128, bf16).  Decode reads the shared pages once per sequence
+    from the block tables; they stay in L2, so logical bytes (as if every
+    sequence held its own copy) move faster than HBM.  The same lengths on
+    unshared pages are timed beside it, and the copy-on-write page copy
+    (pa_copy_pages) on 4096 pages."""
+    import numpy as np
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hq, hkv, D = 32, 8, 128
+    T = prefix + suffix
+    mb = (T + 15) // 16
+    n_pref = prefix // 16
+    n_own = mb - n_pref
+    n_pages = n_pref + B * n_own + B * mb  # shared layout, then an unshared one
+    g = torch.Generator(device=dev).manual_seed(1008)
+    kc = torch.randn(n_pages, hkv, 16, D, generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn(n_pages, hkv, 16, D, generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn(B, hq, D, generator=g, device=dev).to(torch.bfloat16)
+    pool = pa.pa_pool_create(n_pages)
+    try:
+        root = np.full(mb, -1, dtype=np.int32)
+        root[:n_pref] = pa.pa_pool_alloc(pool, n_pref)
+        shared = []
+        for _ in range(B):
+            t = root.copy()
+            pa.pa_pool_share(pool, t[:n_pref])
+            t[n_pref:] = pa.pa_pool_alloc(pool, n_own)
+            shared.append(t)
+        pa.pa_pool_release(pool, root)  # the forks keep the prefix alive
+        unshared = [pa.pa_pool_alloc(pool, mb) for _ in range(B)]
+    finally:
+        pa.pa_pool_destroy(pool)
+    ctx = torch.full((B,), T, dtype=torch.int32, device=dev)
+    out = torch.empty((B, hq, D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def time_it(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    res = {}
+    logical = B * (2 * T * hkv * D * 2 + hq * D * 6)
+    for name, tabs in (("shared", shared), ("unshared", unshared)):
+        bt = torch.from_numpy(np.stack(tabs)).to(dev)
+        ws_bytes = pa.pa_decode_workspace_size(B, hq, hkv, D, 16, mb, 0)
+        ws = torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device=dev)
+        ms = time_it(lambda: pa.pa_decode(q, kc, vc, bt, ctx, out, 1.0 / D ** 0.5, hq, hkv,
+                                          D, 16, B, mb, n_pages, pa.BF16, 0, ws, ws_bytes,
+                                          stream.cuda_stream))
+        res[name] = {"ms_per_step": round(ms, 4),
+                     "logical_GB_s": round(logical / (ms * 1e-3) / 1e9, 1)}
+    unique = (n_pref + B * n_own) * hkv * 16 * D * 2 * 2 + B * hq * D * 6
+    res["shared"]["unique_bytes"] = unique
+    res["shared"]["unique_GB_s"] = round(unique / (res["shared"]["ms_per_step"] * 1e-3) / 1e9, 1)
+    res["logical_bytes_per_step"] = logical
+    res["speedup_vs_unshared"] = round(res["unshared"]["ms_per_step"] /
+                                       res["shared"]["ms_per_step"], 3)
+    # copy-on-write page copy: 4096 pages (pairs disjoint), K and V
+    n_copy = min(4096, n_pages // 2)
+    src = torch.arange(n_copy, dtype=torch.int32, device=dev)
+    dst = src + n_copy
+    ms = time_it(lambda: pa.pa_copy_pages(kc, vc, src, dst, n_copy, hkv, D, 16, n_pages,
+                                          pa.BF16, stream.cuda_stream))
+    moved = 2 * 2 * n_copy * hkv * 16 * D * 2  # read + write, K and V
+    res["copy_pages"] = {"pages": n_copy, "ms": round(ms, 4),
+                         "GB_s": round(moved / (ms * 1e-3) / 1e9, 1),
+                         "frac_of_hbm_peak": round(moved / (ms * 1e-3) / 1e9 /
+                                                   peaks.get("hbm_gbs", 6800.0), 4)}
+    assert pa.pa_last_device_error() == 0
+    res["config"] = f"B={B}, prefix {prefix} shared + {suffix} own tokens, 32/8 heads, D 128, bf16"
+    del kc, vc, q, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_baseline_sample(torch, case, cfg, layers_budget_s=10.0):
     """The float64 oracle, as it stands, on whole layers of the headline
     workload until ~budget seconds pass (at least one layer)."""
@@ -618,6 +703,7 @@ def main_ours(args):
         other["prefill_b4_512over8192"] = run_prefill(torch, pa, workloads, 10, 3, peaks)
         other["verify_gamma4_b4_ctx32k"] = run_verify(torch, pa, workloads, 20, 3, peaks)
         other["window_sink4_w4096_b32_ctx32k"] = run_window(torch, pa, workloads, 20, 3, peaks)
+        other["prefix_shared_b32_8192p128s"] = run_prefix_sharing(torch, pa, 20, 3, peaks)
         for k, v in other.items():
             if "GB_s" in v:
                 v["frac_of_hbm_peak"] = round(v["GB_s"] / hbm, 4)

@@ -64,8 +64,11 @@ enum {
   PA_ERR_BAD_CTX = -12,    /* device: context length < 0 or beyond the table */
   PA_ERR_TIMEOUT = -13,    /* device: a bounded wait for a copy ran out */
   PA_ERR_BAD_INDEX = -14,  /* device: append seq_idx / pos outside the table */
-  PA_ERR_SCRATCH_LIMIT = -15 /* pa_decode_static_workspace: the call needs more
-                                split-K scratch than its fixed 16 MiB array */
+  PA_ERR_SCRATCH_LIMIT = -15, /* pa_decode_static_workspace: the call needs more
+                                 split-K scratch than its fixed 16 MiB array */
+  PA_ERR_POOL_EMPTY = -16,   /* pa_pool_*: not enough free pages (nothing taken) */
+  PA_ERR_POOL_STATE = -17    /* pa_pool_*: a page that is not in use (a double
+                                release, a share of a free page) */
 };
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -260,6 +263,76 @@ int pa_prefill_partition_tokens(int batch, int n_new, int n_q_heads, int n_kv_he
 size_t pa_prefill_workspace_size(int batch, int n_new, int n_q_heads, int n_kv_heads,
                                  int head_dim, int page_size, int max_blocks_per_seq,
                                  int partition_tokens);
+
+/*
+ * Page pool with reference counts, and copy-on-write (prefix sharing).
+ *
+ * PagedAttention lets the block tables of several requests point to the same
+ * physical block; a block shared that way is reference-counted and copied
+ * before one of its users writes into it (ch. 19 "推理系统与性能工程", 19.7.3).
+ * The pool is a host-side allocator of the pages [0, num_pages) of one K/V
+ * cache pair: it counts, per page, the block-table entries that point to it.
+ * The attention entry points read through the tables and need nothing else:
+ * aliased entries are transparent to them.  A pool is an opaque handle owned
+ * by the caller; its functions may be called from several host threads.
+ * Tables passed to the pool are HOST int32 arrays (the caller uploads them).
+ * Every function validates before it changes anything: on an error the pool
+ * is as it was.
+ */
+typedef struct pa_pool pa_pool;
+
+/* A pool of num_pages free pages (NULL if num_pages <= 0 or out of memory). */
+pa_pool *pa_pool_create(int num_pages);
+void pa_pool_destroy(pa_pool *pool);
+
+/* Number of free pages, or PA_ERR_NULL. */
+int pa_pool_free_pages(pa_pool *pool);
+
+/* Block-table entries pointing at `page` (0 = free), or PA_ERR_SHAPE. */
+int pa_pool_refcount(pa_pool *pool, int page);
+
+/* Takes n free pages (reference count 1 each) into pages[0..n); returns
+ * PA_ERR_POOL_EMPTY and takes nothing if fewer than n are free. */
+int pa_pool_alloc(pa_pool *pool, int n, int32_t *pages);
+
+/* One more reference to each page listed (a forked sequence's table now
+ * points to them too); negative entries (unmapped blocks) are skipped.
+ * PA_ERR_POOL_STATE if a listed page is free. */
+int pa_pool_share(pa_pool *pool, const int32_t *pages, int n);
+
+/* One reference fewer to each page listed; a page reaching 0 returns to the
+ * free list.  Negative entries are skipped.  PA_ERR_POOL_STATE if a page
+ * would drop below 0 (a page listed k times needs k references). */
+int pa_pool_release(pa_pool *pool, const int32_t *pages, int n);
+
+/*
+ * Prepares the write of token position `pos` of one sequence whose host
+ * block-table row is table[0 .. max_blocks):
+ *   block pos / page_size unmapped (< 0): a fresh page is mapped; returns 0;
+ *   mapped and used by this table only: nothing to do; returns 0;
+ *   mapped and shared: copy-on-write -- a fresh page is mapped in its place,
+ *     the shared page loses this reference, *copy_src / *copy_dst receive the
+ *     (old, new) pair for pa_copy_pages; returns 1.
+ * *copy_src = *copy_dst = -1 when no copy is due.  Negative PA_ERR_* on bad
+ * arguments, PA_ERR_POOL_EMPTY when no page is free, PA_ERR_POOL_STATE when
+ * the table maps a page the pool holds as free.
+ */
+int pa_pool_prepare_append(pa_pool *pool, int32_t *table, int max_blocks, int page_size,
+                           int pos, int32_t *copy_src, int32_t *copy_dst);
+
+/*
+ * pa_copy_pages -- on the device, copies page src[i] to page dst[i] of both
+ * caches, every kv head (the copy of copy-on-write), for i < n.
+ *   k_cache, v_cache  device [num_pages][n_kv_heads][page_size][head_dim],
+ *                     16-byte aligned
+ *   src, dst          DEVICE int32 [n]; no dst may equal any src (the copies
+ *                     run in parallel)
+ * An out-of-range page skips that pair and records PA_ERR_BAD_BLOCK in the
+ * status word.  Asynchronous on `stream`.
+ */
+int pa_copy_pages(void *k_cache, void *v_cache, const int32_t *src, const int32_t *dst,
+                  int n, int n_kv_heads, int head_dim, int page_size, int num_pages,
+                  pa_dtype dtype, pa_stream_t stream);
 
 /*
  * pa_decode_static_workspace -- pa_decode for callers that cannot allocate.

@@ -23,6 +23,9 @@ __all__ = [
     "pa_merge_partials", "pa_append_kv", "pa_prefill_paged",
     "pa_prefill_paged_split", "pa_prefill_partition_tokens", "pa_prefill_workspace_size",
     "pa_decode_window", "pa_decode_window_workspace_size", "decode_window",
+    "pa_pool_create", "pa_pool_destroy", "pa_pool_free_pages", "pa_pool_refcount",
+    "pa_pool_alloc", "pa_pool_share", "pa_pool_release", "pa_pool_prepare_append",
+    "pa_copy_pages",
     "pa_last_device_error", "pa_strerror", "decode", "prefill", "prefill_split",
     "append_kv",
 ]
@@ -77,6 +80,21 @@ def lib():
         L.pa_decode_window.restype = I
         L.pa_decode_window_workspace_size.argtypes = [I] * 9
         L.pa_decode_window_workspace_size.restype = Z
+        L.pa_pool_create.argtypes = [I]
+        L.pa_pool_create.restype = P
+        L.pa_pool_destroy.argtypes = [P]
+        L.pa_pool_destroy.restype = None
+        L.pa_pool_free_pages.argtypes = [P]
+        L.pa_pool_free_pages.restype = I
+        L.pa_pool_refcount.argtypes = [P, I]
+        L.pa_pool_refcount.restype = I
+        for f in ("pa_pool_alloc", "pa_pool_share", "pa_pool_release"):
+            getattr(L, f).argtypes = [P, I, P] if f == "pa_pool_alloc" else [P, P, I]
+            getattr(L, f).restype = I
+        L.pa_pool_prepare_append.argtypes = [P, P, I, I, I, P, P]
+        L.pa_pool_prepare_append.restype = I
+        L.pa_copy_pages.argtypes = [P, P, P, P] + [I] * 6 + [P]
+        L.pa_copy_pages.restype = I
         L.pa_decode_static_workspace.argtypes = [P, P, P, P, P, P, F] + [I] * 9 + [P]
         L.pa_decode_static_workspace.restype = I
         L.pa_last_device_error.argtypes = [P]
@@ -242,6 +260,78 @@ def pa_decode_window_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, page
     return lib().pa_decode_window_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
                                                  page_size, max_blocks_per_seq, sink_tokens,
                                                  window_tokens, partition_tokens)
+
+
+def _i32_host(a):
+    """A C-contiguous host int32 numpy array (tables and page lists)."""
+    import numpy as np
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    return a, a.ctypes.data
+
+
+def pa_pool_create(num_pages) -> int:
+    """A page pool handle (an opaque pointer as int); raises on failure."""
+    h = lib().pa_pool_create(int(num_pages))
+    if not h:
+        raise PAError(-5, "pa_pool_create")
+    return h
+
+
+def pa_pool_destroy(pool) -> None:
+    lib().pa_pool_destroy(pool)
+
+
+def pa_pool_free_pages(pool) -> int:
+    return lib().pa_pool_free_pages(pool)
+
+
+def pa_pool_refcount(pool, page) -> int:
+    rc = lib().pa_pool_refcount(pool, int(page))
+    if rc < 0:
+        raise PAError(rc, "pa_pool_refcount")
+    return rc
+
+
+def pa_pool_alloc(pool, n):
+    """n fresh pages as an int32 numpy array."""
+    import numpy as np
+    out = np.empty(int(n), dtype=np.int32)
+    _check(lib().pa_pool_alloc(pool, int(n), out.ctypes.data if n else None), "pa_pool_alloc")
+    return out
+
+
+def pa_pool_share(pool, pages) -> int:
+    a, ptr = _i32_host(pages)
+    return _check(lib().pa_pool_share(pool, ptr if a.size else None, a.size), "pa_pool_share")
+
+
+def pa_pool_release(pool, pages) -> int:
+    a, ptr = _i32_host(pages)
+    return _check(lib().pa_pool_release(pool, ptr if a.size else None, a.size),
+                  "pa_pool_release")
+
+
+def pa_pool_prepare_append(pool, table_row, page_size, pos):
+    """table_row: host int32 numpy array, updated in place.  Returns
+    (copy_src, copy_dst): a page pair for pa_copy_pages, or (-1, -1)."""
+    import numpy as np
+    assert isinstance(table_row, np.ndarray) and table_row.dtype == np.int32 \
+        and table_row.flags.c_contiguous
+    src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    rc = lib().pa_pool_prepare_append(pool, table_row.ctypes.data, table_row.size,
+                                      int(page_size), int(pos), ctypes.addressof(src),
+                                      ctypes.addressof(dst))
+    if rc < 0:
+        raise PAError(rc, "pa_pool_prepare_append")
+    return src.value, dst.value
+
+
+def pa_copy_pages(k_cache, v_cache, src, dst, n, n_kv_heads, head_dim, page_size, num_pages,
+                  dtype, stream=None) -> int:
+    rc = lib().pa_copy_pages(_ptr(k_cache), _ptr(v_cache), _ptr(src), _ptr(dst), n,
+                             n_kv_heads, head_dim, page_size, num_pages, dtype,
+                             _stream(stream))
+    return _check(rc, "pa_copy_pages")
 
 
 def pa_last_device_error(stream=None) -> int:

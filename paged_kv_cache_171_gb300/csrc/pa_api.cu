@@ -271,6 +271,8 @@ const char *pa_strerror(int status) {
     case PA_ERR_BAD_INDEX: return "PA_ERR_BAD_INDEX: append seq_idx/pos outside the table";
     case PA_ERR_SCRATCH_LIMIT:
       return "PA_ERR_SCRATCH_LIMIT: needs more split-K scratch than the 16 MiB static array";
+    case PA_ERR_POOL_EMPTY: return "PA_ERR_POOL_EMPTY: not enough free pages in the pool";
+    case PA_ERR_POOL_STATE: return "PA_ERR_POOL_STATE: a page that is not in use";
     default: return "unknown pa status";
   }
 }

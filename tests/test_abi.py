@@ -45,7 +45,7 @@ def test_binding_exposes_same_names():
 
 
 def test_strerror_names_every_status(L):
-    for code in range(0, -16, -1):
+    for code in range(0, -18, -1):
         s = pa.pa_strerror(code)
         assert s and "unknown" not in s, code
     assert "unknown" in pa.pa_strerror(-999)

@@ -21,6 +21,10 @@ Functions and the passages they follow (page title, section):
   prefill         -- 19.3.1 / 19.6.3, causal attention of a chunk of new
                      queries over the cache.
   kv_bytes_*      -- appendix "推理基础" eq. 3 and ch. 19 19.4.2.
+  topm_retain     -- ch. 19 19.4.3 (KV-cache compression, budgeted eviction):
+                     the current position of every (layer, head) is kept, the
+                     other (l, h, t) compete globally by the key
+                     (-score, l, h, t) for the remaining budget.
 """
 from __future__ import annotations
 
@@ -236,3 +240,35 @@ def kv_bytes_per_token(n_layers: int, hidden: int, elem_bytes: int) -> int:
     element size."""
     per_head = 2  # one K vector and one V vector per head, each hidden/H long
     return per_head * hidden * n_layers * elem_bytes
+
+
+def topm_retain(scores, current, budget) -> np.ndarray:
+    """Budgeted global KV retention (ch. 19 19.4.3).
+
+    scores float [L, H, N] (attention mass per layer, head and token);
+    current = C, the generation position; budget = M.  Position C of every
+    (layer, head) is kept unconditionally (L*H slots).  Every other
+    (l, h, t) is a candidate; the candidates are ordered by the key
+    (-score, l, h, t) ascending -- score descending, ties by layer, then head,
+    then token -- and the first M - L*H are kept (none when M <= L*H, all when
+    the budget exceeds them).  -0.0 ranks as 0.0; a NaN score ranks after
+    every number.  Returns bool [L, H, N].
+    """
+    s = np.asarray(scores, dtype=np.float32)
+    L, H, N = s.shape
+    keep = np.zeros((L, H, N), dtype=bool)
+    keep[:, :, current] = True
+    rest = int(budget) - L * H
+    if rest <= 0:
+        return keep
+    l_idx, h_idx, t_idx = np.meshgrid(np.arange(L), np.arange(H), np.arange(N),
+                                      indexing="ij")
+    cand = t_idx.reshape(-1) != current
+    neg = -s.reshape(-1).astype(np.float64)[cand]    # -0.0 and 0.0 compare equal
+    nan_last = np.isnan(neg).astype(np.int8)          # primary key: NaN after every number
+    neg = np.where(np.isnan(neg), 0.0, neg)
+    li, hi, ti = l_idx.reshape(-1)[cand], h_idx.reshape(-1)[cand], t_idx.reshape(-1)[cand]
+    order = np.lexsort((ti, hi, li, neg, nan_last))  # last key is the primary one
+    chosen = order[:rest]
+    keep[li[chosen], hi[chosen], ti[chosen]] = True
+    return keep

@@ -393,3 +393,72 @@ def test_window_hand_derived_case():
                                oracle.BF16, 1, 1)
     e = math.e
     np.testing.assert_allclose(got[0, 0], [1 / (1 + e), e / (1 + e)], rtol=0, atol=1e-15)
+
+
+# --- budgeted global top-M KV retention --------------------------------------
+
+def _naive_topm(scores, current, budget):
+    """The pages' naive method: repeat (budget - L*H) times, scan the whole
+    table for the best remaining candidate (highest score, then lowest
+    layer, head, token)."""
+    L, H, N = scores.shape
+    keep = np.zeros((L, H, N), dtype=bool)
+    keep[:, :, current] = True
+    for _ in range(max(0, budget - L * H)):
+        best = None
+        for l in range(L):
+            for h in range(H):
+                for t in range(N):
+                    if keep[l, h, t]:
+                        continue
+                    s = float(scores[l, h, t])
+                    key = (1 if math.isnan(s) else 0, -s if not math.isnan(s) else 0.0, l, h, t)
+                    if best is None or key < best[0]:
+                        best = (key, (l, h, t))
+        if best is None:
+            break
+        keep[best[1]] = True
+    return keep
+
+
+def test_topm_hand_derived_case():
+    """L=1, H=2, N=4, C=3, M=5: the two current slots, then three of the six
+    candidates: 0.9 (h1, t0); the 0.5 tie goes to head 0 (t2) before head 1
+    (t1); then the other 0.5.  Catches a descending/ascending mix-up and a
+    tie broken the wrong way."""
+    scores = np.array([[[0.1, 0.2, 0.5, 9.0], [0.9, 0.5, 0.3, -1.0]]], dtype=np.float32)
+    keep = oracle.topm_retain(scores, 3, 5)
+    want = np.array([[[False, False, True, True], [True, True, False, True]]])
+    assert np.array_equal(keep, want)
+    keep4 = oracle.topm_retain(scores, 3, 4)  # the tie: head 0 wins
+    assert np.array_equal(keep4, np.array([[[False, False, True, True],
+                                            [True, False, False, True]]]))
+    assert np.array_equal(oracle.topm_retain(scores, 3, 2), scores == scores[..., 3:4])
+    assert oracle.topm_retain(scores, 3, 100).all()
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_topm_equals_the_naive_repeated_scan(seed):
+    """Ties (scores on a coarse grid), -0.0 and +0.0, a NaN: the one global
+    sort equals the pages' naive repeated scan."""
+    rng = np.random.default_rng(seed)
+    L, H, N = 2, 3, 9
+    scores = np.round(rng.normal(size=(L, H, N)) * 2) / 2
+    scores[0, 1, 2] = -0.0
+    scores[1, 0, 5] = 0.0
+    scores[1, 2, 1] = np.nan
+    scores = scores.astype(np.float32)
+    for budget in (0, 5, 6, 7, 20, 40, 54, 60):
+        got = oracle.topm_retain(scores, 4, budget)
+        want = _naive_topm(scores, 4, budget)
+        assert np.array_equal(got, want), budget
+        assert got.sum() == min(max(budget, L * H), L * H * N)
+
+
+def test_topm_counts_differ_per_head():
+    """The budget is global: a head with high scores keeps more tokens."""
+    scores = np.zeros((2, 2, 16), dtype=np.float32)
+    scores[1, 0] = 10.0
+    keep = oracle.topm_retain(scores, 15, 4 + 10)
+    per_head = keep.sum(axis=2)
+    assert per_head[1, 0] == 11 and per_head[0, 0] == 1 and per_head.sum() == 14

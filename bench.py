@@ -588,6 +588,50 @@ def run_prefix_sharing(torch, pa, steps, warmup, peaks, B=32, prefix=8192, suffi
     return res
 
 
+def run_topm(torch, pa, steps, warmup, peaks, L=32, H=32, N=32768):
+    """Budgeted global top-M KV retention at the LLaMA-7B shape (32 layers x
+    32 heads x 32768 tokens = 33.5M scores), budget a quarter of the rows,
+    scores on a 1/16 grid (heavy ties).  Algorithmic bytes = the scores read
+    once + the uint8 mask written; the select reads the scores six times
+    (four radix digits, the tie count, the mask)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev).manual_seed(1009)
+    scores = (torch.randn(L, H, N, generator=g, device=dev) * 16).round() / 16
+    keep = torch.empty((L, H, N), dtype=torch.uint8, device=dev)
+    per_head = torch.empty((L, H), dtype=torch.int32, device=dev)
+    ws_bytes = pa.pa_topm_workspace_size(L, H, N)
+    ws = torch.empty(ws_bytes // 4 + 4, dtype=torch.int32, device=dev)
+    budget = L * H * N // 4
+    stream = torch.cuda.current_stream()
+
+    def once():
+        pa.pa_topm_retain(scores, L, H, N, N - 1, budget, keep, per_head, ws, ws_bytes,
+                          stream.cuda_stream)
+
+    for _ in range(warmup):
+        once()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        once()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    assert pa.pa_last_device_error() == 0 and int(keep.sum()) == budget
+    n = L * H * N
+    algo = n * 4 + n
+    res = {"ms": round(ms, 4), "elements": n, "Gelem_s": round(n / (ms * 1e-3) / 1e9, 2),
+           "algorithmic_GB_s": round(algo / (ms * 1e-3) / 1e9, 1),
+           "frac_of_hbm_peak": round(algo / (ms * 1e-3) / 1e9 / peaks.get("hbm_gbs", 6800.0), 4),
+           "score_passes": 6, "budget": budget,
+           "config": f"{L} layers x {H} heads x {N} tokens, budget 1/4, scores on a 1/16 grid",
+           "l2": "134 MB of scores (above L2); steps timed back to back"}
+    del scores, keep
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_baseline_sample(torch, case, cfg, layers_budget_s=10.0):
     """The float64 oracle, as it stands, on whole layers of the headline
     workload until ~budget seconds pass (at least one layer)."""
@@ -704,6 +748,7 @@ def main_ours(args):
         other["verify_gamma4_b4_ctx32k"] = run_verify(torch, pa, workloads, 20, 3, peaks)
         other["window_sink4_w4096_b32_ctx32k"] = run_window(torch, pa, workloads, 20, 3, peaks)
         other["prefix_shared_b32_8192p128s"] = run_prefix_sharing(torch, pa, 20, 3, peaks)
+        other["topm_retain_l32h32n32k"] = run_topm(torch, pa, 10, 3, peaks)
         for k, v in other.items():
             if "GB_s" in v:
                 v["frac_of_hbm_peak"] = round(v["GB_s"] / hbm, 4)

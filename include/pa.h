@@ -335,6 +335,34 @@ int pa_copy_pages(void *k_cache, void *v_cache, const int32_t *src, const int32_
                   pa_dtype dtype, pa_stream_t stream);
 
 /*
+ * pa_topm_retain -- budgeted global top-M KV retention (ch. 19 "推理系统与
+ * 性能工程", 19.4.3, KV-cache compression by eviction).
+ *
+ * scores[l][h][t] rates the K/V row of token t for layer l, head h (e.g. the
+ * attention mass it received).  Position `current` (C, the generation
+ * position) of every (layer, head) is kept unconditionally: L*H rows.  Every
+ * other (l, h, t) is a candidate, and the candidates compete for the
+ * remaining budget - L*H rows in one global order, key (-score, l, h, t)
+ * ascending: higher score first, ties by lower layer, then head, then token.
+ * The key is a total order, so the kept set is unique.  budget <= L*H keeps
+ * only the current positions; a budget above the candidates keeps all.
+ * -0.0 ranks as 0.0; a NaN score ranks after every number.
+ *   scores         device float [n_layers][n_heads][n_tokens], 16-B aligned
+ *   keep           device uint8 [n_layers][n_heads][n_tokens], 16-B aligned;
+ *                  written: 1 = kept
+ *   kept_per_head  device int32 [n_layers][n_heads] or NULL; written: the
+ *                  kept rows of each (layer, head) (they differ: the budget
+ *                  is global)
+ *   workspace      device, pa_topm_workspace_size bytes, 16-B aligned
+ * PA_ERR_SHAPE for non-positive sizes, more than 2^31 - 2^13 elements, current
+ * outside [0, n_tokens) or a negative budget.  Asynchronous on `stream`.
+ */
+size_t pa_topm_workspace_size(int n_layers, int n_heads, int n_tokens);
+int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens, int current,
+                   long long budget, uint8_t *keep, int32_t *kept_per_head, void *workspace,
+                   size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_decode_static_workspace -- pa_decode for callers that cannot allocate.
  *
  * The pages have no counterpart to this entry point: it is a convenience of

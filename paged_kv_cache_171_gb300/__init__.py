@@ -25,7 +25,7 @@ __all__ = [
     "pa_decode_window", "pa_decode_window_workspace_size", "decode_window",
     "pa_pool_create", "pa_pool_destroy", "pa_pool_free_pages", "pa_pool_refcount",
     "pa_pool_alloc", "pa_pool_share", "pa_pool_release", "pa_pool_prepare_append",
-    "pa_copy_pages",
+    "pa_copy_pages", "pa_topm_retain", "pa_topm_workspace_size", "topm_retain",
     "pa_last_device_error", "pa_strerror", "decode", "prefill", "prefill_split",
     "append_kv",
 ]
@@ -95,6 +95,10 @@ def lib():
         L.pa_pool_prepare_append.restype = I
         L.pa_copy_pages.argtypes = [P, P, P, P] + [I] * 6 + [P]
         L.pa_copy_pages.restype = I
+        L.pa_topm_workspace_size.argtypes = [I, I, I]
+        L.pa_topm_workspace_size.restype = Z
+        L.pa_topm_retain.argtypes = [P, I, I, I, I, ctypes.c_longlong, P, P, P, Z, P]
+        L.pa_topm_retain.restype = I
         L.pa_decode_static_workspace.argtypes = [P, P, P, P, P, P, F] + [I] * 9 + [P]
         L.pa_decode_static_workspace.restype = I
         L.pa_last_device_error.argtypes = [P]
@@ -334,6 +338,18 @@ def pa_copy_pages(k_cache, v_cache, src, dst, n, n_kv_heads, head_dim, page_size
     return _check(rc, "pa_copy_pages")
 
 
+def pa_topm_workspace_size(n_layers, n_heads, n_tokens) -> int:
+    return lib().pa_topm_workspace_size(n_layers, n_heads, n_tokens)
+
+
+def pa_topm_retain(scores, n_layers, n_heads, n_tokens, current, budget, keep,
+                   kept_per_head=None, workspace=None, workspace_bytes=0, stream=None) -> int:
+    rc = lib().pa_topm_retain(_ptr(scores), n_layers, n_heads, n_tokens, current, int(budget),
+                              _ptr(keep), _ptr(kept_per_head), _ptr(workspace),
+                              workspace_bytes, _stream(stream))
+    return _check(rc, "pa_topm_retain")
+
+
 def pa_last_device_error(stream=None) -> int:
     """Synchronises the stream; returns and clears the device status word."""
     return lib().pa_last_device_error(_stream(stream))
@@ -420,3 +436,21 @@ def decode_window(q, k_cache, v_cache, block_table, ctx_lens, scale, sink_tokens
                      B, mb, pages, dtype_code(q), sink_tokens, window_tokens,
                      partition_tokens, workspace, ws_bytes, stream)
     return out
+
+
+def topm_retain(scores, current, budget, keep=None, kept_per_head=None, workspace=None,
+                stream=None):
+    """pa_topm_retain on tensors: scores float32 [L, H, N] on the device.
+    Returns (keep uint8 [L, H, N], kept_per_head int32 [L, H])."""
+    import torch
+    L, H, N = scores.shape
+    if keep is None:
+        keep = torch.empty((L, H, N), dtype=torch.uint8, device=scores.device)
+    if kept_per_head is None:
+        kept_per_head = torch.empty((L, H), dtype=torch.int32, device=scores.device)
+    ws_bytes = pa_topm_workspace_size(L, H, N)
+    if workspace is None:
+        workspace = torch.empty(max(1, ws_bytes // 4), dtype=torch.int32, device=scores.device)
+    pa_topm_retain(scores, L, H, N, current, budget, keep, kept_per_head, workspace, ws_bytes,
+                   stream)
+    return keep, kept_per_head

@@ -197,3 +197,18 @@ def test_decode_window_arguments_and_workspace(L):
         want = _ws_bytes(4, 64, 8, 128, n_parts) if n_parts > 1 else 0
         assert L.pa_decode_window_workspace_size(4, 64, 8, 128, 16, mb, sink, window, pt) == want
     assert L.pa_decode_window_workspace_size(4, 64, 8, 128, 16, mb, -1, 8, 0) == 0
+
+
+def test_topm_arguments(L):
+    P = FAKE
+    ws = L.pa_topm_workspace_size(32, 32, 32768)
+    n = 32 * 32 * 32768
+    assert ws == 256 * 4 + 32 + -(-n // 4096) * 4
+    assert L.pa_topm_workspace_size(0, 1, 1) == 0
+    r = L.pa_topm_retain
+    assert r(None, 2, 2, 8, 0, 5, P, None, P, ws, None) == -1
+    assert r(P, 2, 2, 8, 8, 5, P, None, P, ws, None) == -5     # current outside
+    assert r(P, 2, 2, 8, 0, -1, P, None, P, ws, None) == -5    # negative budget
+    assert r(P, 2, 2, 8, 0, 5, P, None, P, 16, None) == -7     # workspace too small
+    assert r(P + 4, 2, 2, 8, 0, 5, P, None, P, 4096, None) == -8
+    assert r(P, 1 << 16, 1 << 16, 2, 0, 5, P, None, P, 1 << 40, None) == -5

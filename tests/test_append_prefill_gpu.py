@@ -139,3 +139,20 @@ def test_append_then_decode_round_trip():
     torch.cuda.synchronize()
     assert_close(out.cpu().numpy(), ref, "append+decode")
     assert pa.pa_last_device_error() == 0
+
+
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+def test_prefill_negative_and_zero_scale(scale):
+    """The kernel ranks raw scores, so a negative scale is folded into Q's
+    sign and a zero scale becomes a tiny positive factor (every weight 1)."""
+    kw = dict(layers=1, batch=2, n_q_heads=16, n_kv_heads=4, head_dim=128, page_size=16,
+              ctx=[90, 7], dtype="bf16", seed=33, n_new=20, kind="prefill")
+    cpu = workloads.paged_case(**kw)
+    ref = oracle.prefill(cpu.q[0], cpu.k_cache, cpu.v_cache, cpu.block_table[0],
+                         cpu.ctx_lens, scale, cpu.dtype_code)
+    dev = to_device(workloads.paged_case(**kw), "cuda")
+    out = pa.prefill(dev.q[0], dev.k_cache, dev.v_cache, dev.block_table[0], dev.ctx_lens,
+                     scale)
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), ref, f"prefill scale {scale}")
+    assert pa.pa_last_device_error() == 0

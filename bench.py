@@ -821,6 +821,32 @@ def ncu_case(args):
         for _ in range(args.warmup + args.steps):
             pa.prefill(case.q[0], case.k_cache, case.v_cache, case.block_table[0],
                        case.ctx_lens, case.scale)
+    elif args.ncu_case == "verify":  # 4 x 32768 cached + 4 drafted, 64/8 heads
+        case = workloads.paged_case(layers=1, batch=4, n_q_heads=64, n_kv_heads=8,
+                                    head_dim=128, page_size=16, ctx=[32768] * 4, dtype="bf16",
+                                    seed=1006, n_new=4, kind="prefill", device="cuda")
+        for _ in range(args.warmup + args.steps):
+            pa.prefill_split(case.q[0], case.k_cache, case.v_cache, case.block_table[0],
+                             case.ctx_lens, case.scale)
+    elif args.ncu_case == "window":  # 16 x 32768, 64/8 heads, 4 sink + 4096 window
+        case = workloads.paged_case(layers=1, batch=16, n_q_heads=64, n_kv_heads=8,
+                                    head_dim=128, page_size=16, ctx=[32768] * 16, dtype="bf16",
+                                    seed=1007, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            pa.decode_window(case.q[0], case.k_cache, case.v_cache, case.block_table[0],
+                             case.ctx_lens, case.scale, 4, 4096)
+    elif args.ncu_case == "topm":  # 32 x 32 x 32768 scores on a 1/16 grid, budget 1/4
+        g = torch.Generator(device="cuda").manual_seed(1009)
+        sc = (torch.randn(32, 32, 32768, generator=g, device="cuda") * 16).round() / 16
+        for _ in range(args.warmup + args.steps):
+            pa.topm_retain(sc, 32767, 32 * 32 * 32768 // 4)
+    elif args.ncu_case == "copy_pages":  # 4096 page pairs, 8 kv heads, D 128, bf16
+        kc = torch.zeros(8192, 8, 16, 128, dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        src = torch.arange(4096, dtype=torch.int32, device="cuda")
+        dst = src + 4096
+        for _ in range(args.warmup + args.steps):
+            pa.pa_copy_pages(kc, vc, src, dst, 4096, 8, 128, 16, 8192, pa.BF16)
     else:
         name = {"decode": HEADLINE, "decode_gqa8": "gqa8_b4_ctx32k",
                 "decode_gqa4": "gqa4_b64_ragged"}[args.ncu_case]
@@ -843,7 +869,8 @@ def main():
     ap.add_argument("--only-headline", action="store_true",
                     help="skip the other workloads (ragged GQA, 32k split-K, prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["decode", "decode_gqa8", "decode_gqa4",
+    ap.add_argument("--ncu-case", choices=["decode", "decode_gqa8", "decode_gqa4", "verify",
+                                           "window", "topm", "copy_pages",
                                            "prefill"],
                     help="run a small launch sequence for an ncu capture and exit")
     args = ap.parse_args()

@@ -31,6 +31,26 @@
 // and S_x may overwrite P_x.  The running max moves only when a score
 // exceeds it by more than 8 (log2 units).  Every wait is bounded and gives up
 // early once another role has raised the CTA's abort flag.
+//
+// Interleaved key tiles.  When a CTA's queries fit in row tile A (a short
+// chunk, e.g. speculative verify: gamma drafted tokens x GT heads <= 128
+// rows) row tile B takes the same rows, and the two tiles split the key
+// tiles: A the even ones, B the odd ones, so one tile's softmax overlaps the
+// other's MMAs.  Each tile keeps its own (m, l, O) over its keys; at the end
+// B hands (m, l) to A through shared memory, A reads both O's from TMEM (its
+// lanes hold the same rows of O_A and O_B) and merges the two states exactly:
+// O = 2^(m_A - m) O_A + 2^(m_B - m) O_B, l likewise, m = max(m_A, m_B).  Both
+// tiles read Q_A, and Q_B's bytes go to a third V stage.  A stage then serves
+// the two row tiles in turn, so its full and free barriers are kept per (row
+// tile, stage): each is used every lcm(2, stages) tiles by one waiter, in
+// order, and its phase parity stays exact.
+//
+// Split rows.  When an interleaved tile has at most 64 real rows, rows
+// r + 64 of Q repeat rows r, so lanes r and r + 64 of S hold the same scores
+// and their softmax threads compute the same weights.  Lane r writes the head
+// term of P and lane r + 64 the remainder, into the same 64 columns: one
+// P V pass over 128 keys (8 MMAs, not 16) accumulates both, and the row's
+// output is the sum of O's lanes r and r + 64.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_tcgen05.cuh"
@@ -81,25 +101,49 @@ struct TcSmem {
   static constexpr int kK0 = kQ + 2 * kQBytes;
   static constexpr int kV0 = kK0 + kKStages * kKVBytes;
   static constexpr int kBars = kV0 + kVStages * kKVBytes;
-  static constexpr int kSlot = kBars + 40 * 8;  // TMEM address, abort flag
-  static constexpr int kBytes = kSlot + 16;
+  static constexpr int kSlot = kBars + 48 * 8;  // TMEM address, abort flag
+  static constexpr int kML = kSlot + 16;        // interleaved: B's (m, l) per row
+  static constexpr int kBytes = kML + kRows * 8;
+  // Interleaved key tiles: Q_A only, then the K and V rings.
+  static constexpr int kKStagesIl = D == 128 ? 3 : 4;
+  static constexpr int kVStagesIl = D == 128 ? 3 : 4;
+  static constexpr int kK0Il = kQ + kQBytes;
+  static constexpr int kV0Il = kK0Il + kKStagesIl * kKVBytes;
+  static_assert(kV0Il + kVStagesIl * kKVBytes <= kBars, "interleaved rings overflow");
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 232448, "exceeds the per-CTA shared memory limit");
 };
 
-// mbarrier indices
+// mbarrier indices.  Stage barriers come in two sets of 4 (stage s < 4):
+// full barriers use set 0 alone unless interleaved (then set t mod 2); free
+// barriers use set x, the row tile that read the stage.
 enum {
-  kBarK = 0,        // K stage s landed (TMA transaction count), s < 4
-  kBarV = 4,        // V stage s landed
-  kBarKFree = 8,    // K stage s read by row tile x's S MMA (commit), at 8 + 4 x + s
-  kBarVFree = 16,   // V stage s read by row tile x's P V MMAs, at 16 + 4 x + s
-  kBarS = 24,       // S_x of the next key tile in TMEM (commit), per row tile
-  kBarP = 26,       // keys [64 h, 64 h + 64) of P_x in TMEM, at 26 + 2 x + h
+  kBarK = 0,        // K stage s landed (TMA transaction count), at 4 set + s
+  kBarV = 8,        // V stage s landed
+  kBarKFree = 16,   // K stage s read by row tile x's S MMA (commit), at 16 + 4 x + s
+  kBarVFree = 24,   // V stage s read by row tile x's P V MMAs, at 24 + 4 x + s
+  kBarS = 32,       // S_x of the next key tile in TMEM (commit), per row tile
+  kBarP = 34,       // keys [64 h, 64 h + 64) of P_x in TMEM, at 34 + 2 x + h
                     // (one arrival per warp of x's warpgroup)
-  kBarO = 30,       // the last P_x V done (commit, once), per row tile
-  kBarVZ = 32,      // the last V tile's rows past the final key are cleared
-  kBarDrain = 33,   // an MMA warp's own drain on its failure path, per row tile
-  kNumBars = 35
+  kBarO = 38,       // the last P_x V done (commit, once), per row tile
+  kBarVZ = 40,      // the last V tile's rows past the final key are cleared
+  kBarDrain = 41,   // an MMA warp's own drain on its failure path, per row tile
+  kNumBars = 43
+};
+static_assert(kNumBars <= 48, "barrier space");
+
+// Stage bookkeeping for key tile t in a ring of S stages: its stage, the
+// barrier set of its full barrier, and the parity of its use of that
+// barrier.  Interleaved, a barrier of set t mod 2 serves every lcm(2, S)-th
+// tile.
+template <bool IL>
+struct Ring {
+  int S;
+  __device__ __forceinline__ int stage(int t) const { return t % S; }
+  __device__ __forceinline__ int full(int t) const { return (IL ? 4 * (t & 1) : 0) + t % S; }
+  __device__ __forceinline__ uint32_t parity(int t) const {
+    return static_cast<uint32_t>(t / (IL && (S & 1) ? 2 * S : S)) & 1;
+  }
 };
 
 __device__ __forceinline__ uint32_t swz128(int r, int c) {  // row r, 16-B chunk c < 8
@@ -158,10 +202,13 @@ struct TcWork {
   int b, g, hbase, q0;  // batch, kv head, first q head, first query of tile A
   int ctx;              // cached tokens of sequence b
   int part, t0;         // key-range partition, its first key tile
+  int qx[2];            // first query of row tiles A and B
   int nq[2];            // real queries in row tiles A and B (B may have none)
   int n_tiles[2];       // key tiles of the range each row tile visits (0: none)
   int kmax;             // last key any row of the CTA sees (absolute)
-  int n_kv_tiles;       // key tiles loaded = max(n_tiles)
+  int n_kv_tiles;       // key tiles loaded = max(n_tiles), or their sum when il
+  bool il;              // interleaved: B has A's rows; tile x takes tiles t = x mod 2
+  bool sr;              // split rows (interleaved, <= 64 real rows): rows r + 64 repeat r
 };
 
 // Load warps: one copies K, the other V.  Tile t goes into stage t % kStages
@@ -171,15 +218,16 @@ struct TcWork {
 // ahead and checked when used.  The V warp then clears the rows of the last
 // V tile past the final key: P is 0 there, but 0 * (non-finite junk) is NaN
 // in the MMA.
-template <int D>
+template <int D, bool IL>
 __device__ __forceinline__ void load_tiles(bool is_v, const CUtensorMap *map, uint32_t sb,
                                            const int32_t *bt_row, int n_pages, const TcWork &w,
                                            int num_pages, int y_page, int *status,
                                            volatile int *abort_flag, int lane) {
   using L = TcSmem<D>;
-  const int S = is_v ? L::kVStages : L::kKStages;
+  const int S = IL ? (is_v ? L::kVStagesIl : L::kKStagesIl) : (is_v ? L::kVStages : L::kKStages);
+  const Ring<IL> rg{S};
   const int bar_full = is_v ? kBarV : kBarK, bar_free = is_v ? kBarVFree : kBarKFree;
-  const uint32_t ring = sb + (is_v ? L::kV0 : L::kK0);
+  const uint32_t ring = sb + (IL ? (is_v ? L::kV0Il : L::kK0Il) : (is_v ? L::kV0 : L::kK0));
   constexpr int kBoxes = D / 64;
   auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
   auto load_window = [&](int win) {
@@ -204,13 +252,18 @@ __device__ __forceinline__ void load_tiles(bool is_v, const CUtensorMap *map, ui
       idj = 0;
     }
     // the stage's previous tile, t - S, must be released by every row tile
-    // that used it
-    for (int x = 0; x < 2 && ok && t >= S; ++x)
-      if (t - S < w.n_tiles[x])
-        ok = warp_wait(bar(bar_free + 4 * x + t % S), ((t / S) - 1) & 1, abort_flag);
+    // that used it (interleaved: by row tile (t - S) mod 2 alone)
+    if (IL) {
+      const int tp = t - S;
+      if (tp >= 0) ok = warp_wait(bar(bar_free + 4 * (tp & 1) + rg.stage(tp)), rg.parity(tp), abort_flag);
+    } else {
+      for (int x = 0; x < 2 && ok && t >= S; ++x)
+        if (t - S < w.n_tiles[x])
+          ok = warp_wait(bar(bar_free + 4 * x + t % S), ((t / S) - 1) & 1, abort_flag);
+    }
     if (!ok) break;
-    const uint32_t full = bar(bar_full + t % S);
-    const uint32_t dst0 = ring + (t % S) * L::kKVBytes;
+    const uint32_t full = bar(bar_full + rg.full(t));
+    const uint32_t dst0 = ring + rg.stage(t) * L::kKVBytes;
     if (lane == 0) mbar_arrive_expect_tx(full, L::kKVBytes);
     __syncwarp();
     if (lane < 8) {
@@ -225,8 +278,8 @@ __device__ __forceinline__ void load_tiles(bool is_v, const CUtensorMap *map, ui
   const int first = w.kmax - key0 + 1;  // first row of the last V tile no row sees
   if (is_v && ok && n > 0 && first < kKeys) {
     const int t = n - 1;
-    if ((ok = warp_wait(bar(kBarV + t % S), (t / S) & 1, abort_flag))) {
-      const uint32_t vst = ring + (t % S) * L::kKVBytes;
+    if ((ok = warp_wait(bar(kBarV + rg.full(t)), rg.parity(t), abort_flag))) {
+      const uint32_t vst = ring + rg.stage(t) * L::kKVBytes;
       for (int e = lane; e < (kKeys - first) * (D / 8); e += 32) {
         const int rr = first + e / (D / 8), c = e % (D / 8);
         st_shared_v4(vst + (c >> 3) * L::kColBlk + swz128(rr, c), 0u, 0u, 0u, 0u);
@@ -240,7 +293,7 @@ __device__ __forceinline__ void load_tiles(bool is_v, const CUtensorMap *map, ui
     if (lane == 0) raise_abort(status, abort_flag);
     // Copies in flight still land in shared memory: wait for them.
     for (int t = issued > S ? issued - S : 0; t < issued; ++t)
-      mbar_wait(bar(bar_full + t % S), (t / S) & 1);
+      mbar_wait(bar(bar_full + rg.full(t)), rg.parity(t));
   }
 }
 
@@ -249,21 +302,24 @@ __device__ __forceinline__ void load_tiles(bool is_v, const CUtensorMap *map, ui
 // S_x(t+1) goes after P_x(t) V_t because it overwrites P_x in TMEM; MMAs of
 // one thread run in issue order.  With one issuing warp per row tile the
 // tensor pipe takes work from whichever tile is ready, so one tile's
-// barrier waits and softmax do not stall the other's MMAs.
-template <int D, bool BF16>
+// barrier waits and softmax do not stall the other's MMAs.  Interleaved, the
+// j-th key tile of row tile x is t = 2 j + x and both tiles read Q_A.
+template <int D, bool BF16, bool IL, bool SR>
 __device__ __forceinline__ void mma_tiles(int x, uint32_t sb, uint32_t tmem, const TcWork &w,
                                           int *status, volatile int *abort_flag, int lane) {
   using L = TcSmem<D>;
-  constexpr int SK = L::kKStages, SV = L::kVStages;
+  constexpr int SK = IL ? L::kKStagesIl : L::kKStages, SV = IL ? L::kVStagesIl : L::kVStages;
+  const Ring<IL> rk{SK}, rv{SV};
+  constexpr int kStep = IL ? 2 : 1;
   constexpr int KSQ = D / 16;
   constexpr uint32_t kIdS = tc::idesc_f16(BF16, kRows, kKeys, false, false);
   constexpr uint32_t kIdO = tc::idesc_f16(BF16, kRows, D, false, true);
   auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
   // Descriptors of this tile's Q and of stage 0; other stages and K steps add
   // their byte offset >> 4 to the address field.
-  const uint64_t dq = tc::smem_desc_sw128(sb + L::kQ + x * L::kQBytes, 16, 1024);
-  const uint64_t dk0 = tc::smem_desc_sw128(sb + L::kK0, 16, 1024);
-  const uint64_t dv0 = tc::smem_desc_sw128(sb + L::kV0, L::kColBlk, 1024);
+  const uint64_t dq = tc::smem_desc_sw128(sb + L::kQ + (IL ? 0 : x * L::kQBytes), 16, 1024);
+  const uint64_t dk0 = tc::smem_desc_sw128(sb + (IL ? L::kK0Il : L::kK0), 16, 1024);
+  const uint64_t dv0 = tc::smem_desc_sw128(sb + (IL ? L::kV0Il : L::kV0), L::kColBlk, 1024);
   const uint32_t tSx = tmem + x * kKeys, tOx = tmem + 2 * kKeys + x * D;
   const int n = w.n_kv_tiles, nx = w.n_tiles[x];
   const int last_first = w.kmax - (w.t0 + n - 1) * kKeys + 1;
@@ -284,46 +340,51 @@ __device__ __forceinline__ void mma_tiles(int x, uint32_t sb, uint32_t tmem, con
   };
   // O_x += P_x[:, keys of half h] V_t[keys of half h].  P_x in TMEM: head
   // terms in columns 0-63 (two keys per column), remainders in 64-127.
-  auto pv_mma = [&](int t, int h) {
+  auto pv_mma = [&](int j, int t, int h) {  // the j-th key tile of x is t
     if (lane == 0) {
       const uint64_t dv = dv0 + static_cast<uint64_t>(((t % SV) * L::kKVBytes) >> 4);
       const uint32_t pa = tSx + 32 * h;
+      constexpr int n_ph = SR ? 1 : 2;  // split rows: the remainders are in rows 64-127
 #pragma unroll
       for (int ph = 0; ph < 2; ++ph) {
+        if (ph >= n_ph) break;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc::mma_f16_tmem_a(tOx, pa + 64 * ph + 8 * kk,
                              dv + static_cast<uint64_t>(((4 * h + kk) * 2048) >> 4), kIdO,
-                             (t > 0 || h > 0 || ph > 0 || kk > 0) ? 1u : 0u);
+                             (j > 0 || h > 0 || ph > 0 || kk > 0) ? 1u : 0u);
       }
       if (h == 1) {
         tc::commit(bar(kBarVFree + 4 * x + t % SV));
-        if (t == nx - 1) tc::commit(bar(kBarO + x));
+        if (j == nx - 1) tc::commit(bar(kBarO + x));
       }
     }
     __syncwarp();
   };
 
   bool ok = true;
-  if (nx > 0 && (ok = warp_wait(bar(kBarK), 0, abort_flag))) {
+  const int tx = IL ? x : 0;  // x's first key tile
+  if (nx > 0 && (ok = warp_wait(bar(kBarK + rk.full(tx)), rk.parity(tx), abort_flag))) {
     tc::fence_after_sync();
-    s_mma(0);
+    s_mma(tx);
   }
-  for (int t = 0; t < nx && ok; ++t) {
+  for (int j = 0; j < nx && ok; ++j) {
+    const int t = tx + kStep * j;
     for (int h = 0; h < 2 && ok; ++h) {
-      if (!(ok = warp_wait(bar(kBarP + 2 * x + h), t & 1, abort_flag))) break;
+      if (!(ok = warp_wait(bar(kBarP + 2 * x + h), j & 1, abort_flag))) break;
       if (h == 0) {
         ok = (t == n - 1 && cleared) ? warp_wait(bar(kBarVZ), 0, abort_flag)
-                                     : warp_wait(bar(kBarV + t % SV), (t / SV) & 1, abort_flag);
+                                     : warp_wait(bar(kBarV + rv.full(t)), rv.parity(t), abort_flag);
         if (!ok) break;
       }
       tc::fence_after_sync();
-      pv_mma(t, h);
+      pv_mma(j, t, h);
     }
-    if (ok && t + 1 < nx &&
-        (ok = warp_wait(bar(kBarK + (t + 1) % SK), ((t + 1) / SK) & 1, abort_flag))) {
+    const int tn = t + kStep;
+    if (ok && j + 1 < nx &&
+        (ok = warp_wait(bar(kBarK + rk.full(tn)), rk.parity(tn), abort_flag))) {
       tc::fence_after_sync();
-      s_mma(t + 1);
+      s_mma(tn);
     }
   }
   if (!ok) {
@@ -336,18 +397,36 @@ __device__ __forceinline__ void mma_tiles(int x, uint32_t sb, uint32_t tmem, con
   }
 }
 
-// Softmax warpgroup x (warps 4 + 4 x .. 7 + 4 x): lane l of warp w owns row
-// r = 32 (w % 4) + l of row tile x, i.e. query q0 + x BQ + r / GT, head
-// hbase + r % GT, and TMEM lane r.
-template <int D, int GT, bool BF16>
+// Named barriers of the softmax warps.  Barrier 1 joins warps 4-11 and
+// returns whether any thread passed true; barrier 2 joins warps 4-7.
+__device__ __forceinline__ bool softmax_pair_sync_any(bool c) {
+  uint32_t any;
+  asm volatile(
+      "{\n\t.reg .pred q, p;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 256, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(any)
+      : "r"(static_cast<uint32_t>(c))
+      : "memory");
+  return any != 0;
+}
+__device__ __forceinline__ void softmax_group_sync() {
+  asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
+// Softmax warpgroup x (warps 4 + 4 x .. 7 + 4 x): lane l of warp w owns TMEM
+// lane r = 32 (w % 4) + l of row tile x, i.e. row rr = r (split rows:
+// r mod 64): query qx[x] + rr / GT, head hbase + rr % GT.
+template <int D, int GT, bool BF16, bool IL, bool SR>
 __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const TcParams &p,
                                               const TcWork &w, volatile int *abort_flag,
-                                              int x, int warp, int lane) {
+                                              float *ml, float *scratch, int x, int warp,
+                                              int lane) {
   using L = TcSmem<D>;
-  constexpr int BQ = kRows / GT;
   auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
-  const int r = ((warp & 3) << 5) + lane, qi = r / GT, hh = r % GT;
-  const int qx0 = w.q0 + x * BQ;
+  const int r = ((warp & 3) << 5) + lane, rr = SR ? (r & 63) : r;
+  const int qi = rr / GT, hh = rr % GT;
+  const bool rem = SR && r >= 64;  // this warp writes the remainder terms
+  const int qx0 = w.qx[x];
   const int kmax_x = w.ctx + qx0 + w.nq[x] - 1;
   const int lim = min(w.ctx + qx0 + qi, kmax_x);  // last key row r sees
   const int lim_all = w.ctx + qx0;                // every row of x sees keys <= this
@@ -372,7 +451,7 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
     tc::wait_ld();
 
     // ---- mask, max of the raw scores, lazy move of the reference max
-    const int key0 = (w.t0 + j) * kKeys;
+    const int key0 = (w.t0 + (IL ? 2 * j + x : j)) * kKeys;
     if (key0 + kKeys - 1 > lim_all) {
       const int last = lim - key0;  // keys past this one are masked for row r
 #pragma unroll
@@ -414,8 +493,12 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
         const float2 hr = unpack2<BF16>(phi[k]);
         plo[k] = pack2<BF16>(p0 - hr.x, p1 - hr.y);
       }
-      tc::st16(tSx + 16 * ch, phi);
-      tc::st16(tSx + 64 + 16 * ch, plo);
+      if (!SR) {
+        tc::st16(tSx + 16 * ch, phi);
+        tc::st16(tSx + 64 + 16 * ch, plo);
+      } else {
+        tc::st16(tSx + 16 * ch, rem ? plo : phi);
+      }
       if (ch == 1 && j > 0 && __any_sync(kFull, need)) {
         // the max moved: rescale this row of O_x before the first P V of
         // this tile (P_x V_{j-1} has completed: S_x was issued after it)
@@ -440,30 +523,89 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
   tc::wait_st();
   if (nt == 0) return;
   if (!bad) bad = !warp_wait(bar(kBarO + x), 0, abort_flag);
-  if (bad) {
-    if (lane == 0) raise_abort(p.status, abort_flag);
+  if (bad && lane == 0) raise_abort(p.status, abort_flag);
+  float l = l0 + l1, ca = 1.f, cb = 0.f;
+  if (IL) {
+    // both warpgroups always meet here, failed or not, and all of them take
+    // the same decision
+    if (x == 1) {
+      ml[2 * r] = m;
+      ml[2 * r + 1] = l;
+    }
+    if (softmax_pair_sync_any(bad || *abort_flag) || x == 1) return;
+    const float mb = ml[2 * r], lb = ml[2 * r + 1];
+    const float mn = fmaxf(m, mb);
+    if (mn != -INFINITY) {  // else no key reached this row: O and l stay 0
+      ca = ex2(m - mn);
+      cb = ex2(mb - mn);
+    }
+    m = mn;
+    l = ca * l + cb * lb;
+  } else if (bad) {
     return;
   }
   tc::fence_after_sync();
 
   // ---- O / l for this row, or the row's partial state for this key range
-  const float l = l0 + l1;
   const bool split = p.n_parts > 1;
   const float inv = split ? 1.f : (l > 0.f ? 1.f / l : 0.f);
   const size_t row =
       (static_cast<size_t>(w.b) * p.n_new + qx0 + qi) * p.n_q_heads + w.hbase + hh;
   float *dst = split ? p.ws + (row * p.n_parts + w.part) * (D + 4) : p.out + row * D;
+  // columns 32 c .. 32 c + 31 of this lane's O (interleaved: both tiles' merged)
+  auto load_o = [&](int c, uint32_t (&o)[32]) {
+    tc::ld32(tOx + c * 32, o);
+    if (IL) {  // O_A 2^(m_A - m) + O_B 2^(m_B - m); O_B is D columns to the right
+      uint32_t ob[32];
+      tc::ld32(tOx + D + c * 32, ob);
+      tc::wait_ld();
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        o[k] = __float_as_uint(ca * __uint_as_float(o[k]) + cb * __uint_as_float(ob[k]));
+    } else {
+      tc::wait_ld();
+    }
+  };
+  // Split rows: lane rr + 64 hands its part of O to lane rr through shared
+  // memory (Q_A's space, free once every S MMA has completed); float4 k of
+  // row rr sits at slot k ^ (rr mod 8).
+  auto scr = [&](int k4) { return scratch + rr * D + ((k4 ^ (rr & 7)) << 2); };
+  if (SR) {
+    if (rem) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        load_o(c, o);
+#pragma unroll
+        for (int k = 0; k < 32; k += 4)
+          *reinterpret_cast<float4 *>(scr(c * 8 + k / 4)) =
+              make_float4(__uint_as_float(o[k]), __uint_as_float(o[k + 1]),
+                          __uint_as_float(o[k + 2]), __uint_as_float(o[k + 3]));
+      }
+    }
+    softmax_group_sync();  // warps 4-7: all reach it (the decision above is shared)
+    if (rem) return;
+  }
   if (split && qi < w.nq[x])
     *reinterpret_cast<float2 *>(dst + D) = make_float2(m * kLn2, l);  // natural-log m
 #pragma unroll
-  for (int cb = 0; cb < D / 32; ++cb) {
+  for (int c = 0; c < D / 32; ++c) {
     uint32_t o[32];
-    tc::ld32(tOx + cb * 32, o);
-    tc::wait_ld();
+    load_o(c, o);
+    if (SR) {
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(scr(c * 8 + k / 4));
+        o[k] = __float_as_uint(__uint_as_float(o[k]) + t.x);
+        o[k + 1] = __float_as_uint(__uint_as_float(o[k + 1]) + t.y);
+        o[k + 2] = __float_as_uint(__uint_as_float(o[k + 2]) + t.z);
+        o[k + 3] = __float_as_uint(__uint_as_float(o[k + 3]) + t.w);
+      }
+    }
     if (qi < w.nq[x]) {
 #pragma unroll
       for (int k = 0; k < 32; k += 4)
-        *reinterpret_cast<float4 *>(dst + cb * 32 + k) =
+        *reinterpret_cast<float4 *>(dst + c * 32 + k) =
             make_float4(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
                         __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
     }
@@ -508,6 +650,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (w.nq[x] > 0) w.kmax = max(w.kmax, kx);
   }
   w.n_kv_tiles = max(w.n_tiles[0], w.n_tiles[1]);
+  // B idle and A with at least two key tiles: interleave (B gets the odd ones)
+  w.il = w.nq[1] == 0 && w.n_tiles[0] >= 2;
+  w.qx[0] = w.q0;
+  w.qx[1] = w.il ? w.q0 : w.q0 + BQ;
+  if (w.il) {
+    w.nq[1] = w.nq[0];
+    w.n_tiles[1] = w.n_tiles[0] / 2;
+    w.n_tiles[0] -= w.n_tiles[1];
+  }
+  w.sr = w.il && w.nq[0] * GT <= kRows / 2;
   const int n_pages = (ctx + p.n_new + 15) >> 4;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kSlot + 4);
 
@@ -522,18 +674,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::alloc(sb + L::kSlot, 512);
     tc::relinquish();
   }
-  // Q tiles: row r of tile x = query q0 + x BQ + r / GT, head hbase + r % GT
-  // (zeros past the chunk's end; the sign of a negative scale folded in)
-  if (warp >= kSoftmaxWarp0) {
+  // Q tiles: row r of tile x = query qx[x] + r / GT, head hbase + r % GT
+  // (zeros past the chunk's end; the sign of a negative scale folded in).
+  // Interleaved, only Q_A is loaded: Q_B's space belongs to the K ring.
+  if (warp >= kSoftmaxWarp0 && !(w.il && warp >= kSoftmaxWarp0 + 4)) {
     const int x = (warp - kSoftmaxWarp0) >> 2;
     for (int e = tid & 127; e < kRows * (D / 8); e += 128) {
       const int r = e / (D / 8), c = e % (D / 8);
-      const int qi = r / GT, hh = r % GT;
+      const int rr = w.sr ? (r & 63) : r;  // split rows: rows 64-127 repeat 0-63
+      const int qi = rr / GT, hh = rr % GT;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (qi < w.nq[x]) {
         v = *reinterpret_cast<const uint4 *>(
             p.q +
-            ((static_cast<size_t>(w.b) * p.n_new + w.q0 + x * BQ + qi) * p.n_q_heads +
+            ((static_cast<size_t>(w.b) * p.n_new + w.qx[x] + qi) * p.n_q_heads +
              w.hbase + hh) * D + c * 8);
         v.x ^= p.qsign;
         v.y ^= p.qsign;
@@ -552,14 +706,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kKLoadWarp || warp == kVLoadWarp) {
     const bool is_v = warp == kVLoadWarp;
-    load_tiles<D>(is_v, is_v ? &vmap : &kmap, sb,
-                  p.block_table + static_cast<size_t>(w.b) * p.max_blocks, n_pages, w,
-                  p.num_pages, p.n_kv_heads * 16, p.status, abort_flag, lane);
+    const int32_t *bt_row = p.block_table + static_cast<size_t>(w.b) * p.max_blocks;
+    if (w.il)
+      load_tiles<D, true>(is_v, is_v ? &vmap : &kmap, sb, bt_row, n_pages, w, p.num_pages,
+                          p.n_kv_heads * 16, p.status, abort_flag, lane);
+    else
+      load_tiles<D, false>(is_v, is_v ? &vmap : &kmap, sb, bt_row, n_pages, w, p.num_pages,
+                           p.n_kv_heads * 16, p.status, abort_flag, lane);
   } else if (warp < 2) {
-    mma_tiles<D, BF16>(warp, sb, tmem, w, p.status, abort_flag, lane);
+    if (w.sr)
+      mma_tiles<D, BF16, true, true>(warp, sb, tmem, w, p.status, abort_flag, lane);
+    else if (w.il)
+      mma_tiles<D, BF16, true, false>(warp, sb, tmem, w, p.status, abort_flag, lane);
+    else
+      mma_tiles<D, BF16, false, false>(warp, sb, tmem, w, p.status, abort_flag, lane);
   } else if (warp >= kSoftmaxWarp0) {
-    softmax_tiles<D, GT, BF16>(sb, tmem, p, w, abort_flag, (warp - kSoftmaxWarp0) >> 2, warp,
-                               lane);
+    float *ml = reinterpret_cast<float *>(smem + L::kML);
+    float *scratch = reinterpret_cast<float *>(smem + L::kQ);
+    const int x = (warp - kSoftmaxWarp0) >> 2;
+    if (w.sr)
+      softmax_tiles<D, GT, BF16, true, true>(sb, tmem, p, w, abort_flag, ml, scratch, x, warp,
+                                             lane);
+    else if (w.il)
+      softmax_tiles<D, GT, BF16, true, false>(sb, tmem, p, w, abort_flag, ml, scratch, x, warp,
+                                              lane);
+    else
+      softmax_tiles<D, GT, BF16, false, false>(sb, tmem, p, w, abort_flag, ml, scratch, x,
+                                               warp, lane);
   }
   tc::fence_before_sync();
   __syncthreads();

@@ -31,6 +31,10 @@ def _built():
     (64, 12, 4, "fp16", [1, 250], 33, 128),
     (128, 64, 8, "bf16", [300], 1, 128),               # one query: decode
     (128, 16, 2, "bf16", [2047, 2048, 2049], 3, 1024), # ctx at partition edges
+    (128, 64, 8, "bf16", [126, 127, 129], 4, 0),       # odd key tile unseen by some rows
+    (128, 64, 8, "bf16", [900, 3000], 8, 0),           # 64 rows: head/remainder row halves
+    (128, 64, 8, "fp16", [900, 3000], 9, 0),           # 72 rows: interleaved tiles only
+    (64, 32, 4, "bf16", [700, 2100], 16, 0),           # 64 rows at D 64
 ])
 def test_split_prefill_small_shapes(head_dim, hq, hkv, dtype, cached, n_new, part):
     kw = dict(layers=1, batch=len(cached), n_q_heads=hq, n_kv_heads=hkv,

@@ -21,7 +21,12 @@
 //   O_x  += P_x V_j            tcgen05.mma with A in TMEM, B in shared memory
 // The tensor pipe alternates between the two row tiles: while tile A's
 // softmax runs it computes P_B V_j and S_B for the next key tile, and the
-// other way round.
+// other way round.  The softmax warpgroups enforce that ping-pong: B's
+// softmax of key tile j starts once A has handed over P_A(j), and A's of
+// tile j+1 once B has handed over P_B(j).  Left to themselves the two tiles
+// fall into lockstep (their S MMAs finish together), both softmaxes then
+// share the SM sub-partitions while the tensor pipe idles, and a key tile
+// takes the sum of both phases instead of the larger.
 //
 // Warp roles: warps 0 and 1 issue the MMAs of row tiles A and B (one thread
 // each), warps 2 and 3 the K and V TMA loads, warps 4-7 are tile A's softmax
@@ -439,6 +444,16 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
   bool bad = false;
   float m = -INFINITY, l0 = 0.f, l1 = 0.f;
   for (int j = 0; j < nt; ++j) {
+    // ping-pong: wait for the other tile's turn before this one (where the
+    // other tile has that many key tiles)
+    const int jo = j - 1 + x;
+    if (jo >= 0 && jo < w.n_tiles[x ^ 1]) {
+      if (!warp_wait(bar(kBarP + 2 * (x ^ 1)), jo & 1, abort_flag) ||
+          !warp_wait(bar(kBarP + 2 * (x ^ 1) + 1), jo & 1, abort_flag)) {
+        bad = true;
+        break;
+      }
+    }
     if (!warp_wait(bar(kBarS + x), j & 1, abort_flag)) {
       bad = true;
       break;

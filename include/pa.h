@@ -353,9 +353,13 @@ int pa_copy_pages(void *k_cache, void *v_cache, const int32_t *src, const int32_
  *   kept_per_head  device int32 [n_layers][n_heads] or NULL; written: the
  *                  kept rows of each (layer, head) (they differ: the budget
  *                  is global)
- *   workspace      device, pa_topm_workspace_size bytes, 16-B aligned
+ *   workspace      device, pa_topm_workspace_size bytes, 16-B aligned: about
+ *                  8 bytes per element (the select's candidate list, an index
+ *                  and a key, can hold every element) plus 21 KiB and 4 bytes
+ *                  per 4096 elements
  * PA_ERR_SHAPE for non-positive sizes, more than 2^31 - 2^13 elements, current
- * outside [0, n_tokens) or a negative budget.  Asynchronous on `stream`.
+ * outside [0, n_tokens) or a negative budget; PA_ERR_WORKSPACE when
+ * workspace_bytes is below pa_topm_workspace_size.  Asynchronous on `stream`.
  */
 size_t pa_topm_workspace_size(int n_layers, int n_heads, int n_tokens);
 int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens, int current,

@@ -11,14 +11,20 @@
 // key f(score) whose ascending order is descending score (-0.0 as 0.0, NaN
 // after every number); the (l, h, t) part is the element's index in the
 // [L][H][N] array, so index order already is the tie order.  A radix select
-// over f (four 8-bit digits, most significant first; each digit one
-// histogram pass over the scores plus a one-CTA pick) finds the key S* of the
-// K-th candidate and its rank r among the candidates whose key equals S*.
-// The kept candidates are then exactly: f < S*, plus the first r with f = S*
-// in index order.  The r-th of those is located by counting ties per chunk of
-// the array, scanning the counts to find its chunk, and ranking that one
-// chunk's ties; with its index idx*, the final pass keeps (f, index) <=
-// (S*, idx*) -- a plain comparison per element.
+// over f (digits of 11, 11 and 10 bits, most significant first) finds the key
+// S* of the K-th candidate and its rank r among the candidates whose key
+// equals S*.  The kept candidates are then exactly: f < S*, plus the first r
+// with f = S* in index order.
+//
+// Only two passes stream the scores.  The first histograms the top 11 bits
+// and a one-CTA pick finds the bucket b1 holding the K-th key.  The second
+// settles every element outside b1 (kept if its bucket is below b1, dropped
+// if above), writes the keep mask and appends the (index, key) of b1's
+// elements to a candidate list.  The remaining digits, the tie rank and the
+// final keeps then run over the candidates alone:
+// the r-th tie is located by counting ties per chunk of the array, scanning
+// the counts to find its chunk, and ranking that one chunk's ties; with its
+// index idx*, a candidate is kept when (f, index) <= (S*, idx*).
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -29,7 +35,10 @@ constexpr int kThreads = 256;
 constexpr int kPerThread = 16;                     // consecutive elements per thread
 constexpr int kChunk = kThreads * kPerThread;      // elements per chunk (final passes)
 
-// The state of the select, in the workspace after the histogram.
+constexpr int kBins1 = 2048, kBins2 = 2048, kBins3 = 1024;  // digits of 11, 11, 10 bits
+constexpr int kShift1 = 21, kShift2 = 10;
+
+// The state of the select, in the workspace after the histograms.
 struct TopmState {
   uint32_t prefix;     // key bits decided so far (S* at the end)
   uint32_t mask;       // which bits are decided
@@ -37,7 +46,8 @@ struct TopmState {
   uint32_t tie_chunk;  // chunk holding the k_rem-th candidate with key S*
   uint32_t tie_rank;   // its 1-based rank among that chunk's ties
   uint32_t idx_star;   // its index: the last kept candidate
-  uint32_t pad[2];
+  uint32_t n_cand;     // elements of bucket b1 appended to the candidate list
+  uint32_t pad;
 };
 
 // Ascending f <=> descending score; -0.0 as 0.0; NaN after every number.
@@ -48,10 +58,13 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return ~u;                                        // descending
 }
 
+// Zeroes the three histograms and the per-chunk tie counts, sets the state.
 __global__ void __launch_bounds__(kThreads)
-    topm_init_kernel(uint32_t *__restrict__ hist, TopmState *__restrict__ st, uint32_t k) {
-  hist[threadIdx.x] = 0;
-  if (threadIdx.x == 0) *st = TopmState{0u, 0u, k, 0u, 0u, 0u, {0u, 0u}};
+    topm_init_kernel(uint32_t *__restrict__ hist, int n_zero, TopmState *__restrict__ st,
+                     uint32_t k) {
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < n_zero; i += gridDim.x * kThreads)
+    hist[i] = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *st = TopmState{0u, 0u, k, 0u, 0u, 0u, 0u, 0u};
 }
 
 // The kPerThread consecutive scores from `base` (16-byte aligned when the
@@ -73,18 +86,17 @@ __device__ __forceinline__ void load_run(const float *__restrict__ scores, int n
   }
 }
 
-// Histogram of digit (key >> shift) & 255 over the candidates whose decided
-// bits match the prefix.  Each warp counts into its own shared histogram.
+// First digit: histogram of the top 11 key bits over every candidate
+// element.  Each quarter of the CTA's warps counts into its own copy in
+// shared memory (fewer collisions on the few crowded bins), summed at the end.
 __global__ void __launch_bounds__(kThreads)
-    topm_hist_kernel(const float *__restrict__ scores, int n, int N, int current,
-                     uint32_t *__restrict__ hist, const TopmState *__restrict__ st,
-                     int shift) {
-  constexpr int NW = kThreads / 32;
-  __shared__ uint32_t h[NW][256];
-  for (int i = threadIdx.x; i < NW * 256; i += kThreads) h[i / 256][i % 256] = 0;
+    topm_hist1_kernel(const float *__restrict__ scores, int n, int N, int current,
+                      uint32_t *__restrict__ hist) {
+  constexpr int kCopies = 4;
+  __shared__ uint32_t h[kCopies][kBins1];
+  for (int i = threadIdx.x; i < kCopies * kBins1; i += kThreads) h[i / kBins1][i % kBins1] = 0;
   __syncthreads();
-  const uint32_t prefix = st->prefix, mask = st->mask;
-  const int warp = threadIdx.x >> 5;
+  uint32_t *mine = h[(threadIdx.x >> 5) & (kCopies - 1)];
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kChunk;
   for (int64_t cbase = static_cast<int64_t>(blockIdx.x) * kChunk; cbase < n; cbase += stride) {
     const int base = static_cast<int>(cbase) + threadIdx.x * kPerThread;
@@ -93,72 +105,229 @@ __global__ void __launch_bounds__(kThreads)
     int t = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
 #pragma unroll
     for (int e = 0; e < kPerThread; ++e) {
-      uint32_t bin = 256u;  // none
-      if (base + e < n && t != current) {
-        const uint32_t k = score_key(sc[e]);
-        if ((k & mask) == prefix) bin = (k >> shift) & 255u;
-      }
-      if (bin != 256u) atomicAdd(&h[warp][bin], 1u);
+      if (base + e < n && t != current) atomicAdd(&mine[score_key(sc[e]) >> kShift1], 1u);
       if (++t == N) t = 0;
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 256; i += kThreads) {
+  for (int i = threadIdx.x; i < kBins1; i += kThreads) {
     uint32_t v = 0;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) v += h[w][i];
+    for (int c = 0; c < kCopies; ++c) v += h[c][i];
     if (v) atomicAdd(&hist[i], v);
   }
 }
 
-// One CTA: the bucket holding the k_rem-th key; clears the histogram.
-__global__ void __launch_bounds__(kThreads)
+// One CTA of 1024 threads: the bin of `hist` (BINS bins, digit at `shift`)
+// holding the k_rem-th key of the current bucket; clears the histogram.
+template <int BINS>
+__global__ void __launch_bounds__(1024)
     topm_pick_kernel(uint32_t *__restrict__ hist, TopmState *__restrict__ st, int shift) {
-  __shared__ uint32_t c[256];
+  constexpr int kPer = BINS / 1024;
+  __shared__ uint32_t c[1024];
   const int t = threadIdx.x;
-  c[t] = hist[t];
+  uint32_t v[kPer], sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    v[i] = hist[kPer * t + i];
+    sum += v[i];
+  }
+  c[t] = sum;
   __syncthreads();
-  // inclusive scan (Hillis-Steele) over the 256 bins
-  for (int o = 1; o < 256; o <<= 1) {
-    const uint32_t v = t >= o ? c[t - o] : 0u;
+  for (int o = 1; o < 1024; o <<= 1) {  // inclusive scan (Hillis-Steele)
+    const uint32_t u = t >= o ? c[t - o] : 0u;
     __syncthreads();
-    c[t] += v;
+    c[t] += u;
     __syncthreads();
   }
   const uint32_t k = st->k_rem;
-  const uint32_t before = t > 0 ? c[t - 1] : 0u;
-  if (before < k && k <= c[t]) {  // exactly one bin
-    st->k_rem = k - before;
-    st->prefix |= static_cast<uint32_t>(t) << shift;
-    st->mask |= 0xFFu << shift;
+  uint32_t before = c[t] - sum;
+  if (before < k && k <= c[t]) {  // exactly one thread
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if (before < k && k <= before + v[i]) {
+        st->k_rem = k - before;
+        st->prefix |= static_cast<uint32_t>(kPer * t + i) << shift;
+        st->mask |= static_cast<uint32_t>(BINS - 1) << shift;
+      }
+      before += v[i];
+    }
   }
-  hist[t] = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) hist[kPer * t + i] = 0;
 }
 
-// Candidates whose key equals S*, per chunk of kChunk elements.
-__global__ void __launch_bounds__(kThreads)
-    topm_tiecount_kernel(const float *__restrict__ scores, int n, int N, int current,
-                         const TopmState *__restrict__ st, uint32_t *__restrict__ tiecnt) {
-  const uint32_t skey = st->prefix;
-  const int base = blockIdx.x * kChunk + threadIdx.x * kPerThread;
+// Second pass over the scores.  Every element outside bucket b1 is settled:
+// kept (current position, or a bucket below b1) or dropped; b1's elements
+// are written 0 here and appended to the candidate list.  Kept rows per
+// (layer, head) are summed in shared memory, then added once per CTA.
+__global__ void __launch_bounds__(kThreads, 8)
+    topm_split_kernel(const float *__restrict__ scores, int n, int N, int current,
+                      TopmState *__restrict__ st, uint8_t *__restrict__ keep,
+                      int32_t *__restrict__ per_head, uint32_t *__restrict__ cand,
+                      uint32_t *__restrict__ ckey) {
+  __shared__ int cnt[kChunk + 2];  // rows of this chunk, relative to its first
+  const uint32_t b1 = st->prefix >> kShift1;
+  const int cbase = blockIdx.x * kChunk;
+  const int row0 = static_cast<int>(static_cast<unsigned>(cbase) / static_cast<unsigned>(N));
+  const int cend = min(n, cbase + kChunk);
+  const int n_rows =
+      static_cast<int>(static_cast<unsigned>(cend - 1) / static_cast<unsigned>(N)) - row0 + 1;
+  if (per_head) {
+    for (int i = threadIdx.x; i < n_rows; i += kThreads) cnt[i] = 0;
+    __syncthreads();
+  }
+  const int base = cbase + threadIdx.x * kPerThread;
   float sc[kPerThread];
   load_run(scores, n, base, sc);
   int t = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
-  uint32_t cnt = 0;
+  int row = static_cast<int>(static_cast<unsigned>(base) / static_cast<unsigned>(N)) - row0;
+  int run_row = -1, run = 0;  // kept count of the current (layer, head) run
+  uint32_t bytes[kPerThread / 4] = {0u, 0u, 0u, 0u};
+  uint32_t cbits = 0;  // bit e: element base + e is a candidate
 #pragma unroll
   for (int e = 0; e < kPerThread; ++e) {
-    cnt += base + e < n && t != current && score_key(sc[e]) == skey;
-    if (++t == N) t = 0;
+    if (base + e < n) {
+      const uint32_t bk = score_key(sc[e]) >> kShift1;
+      const bool k = t == current || bk < b1;
+      if (t != current && bk == b1) cbits |= 1u << e;
+      bytes[e >> 2] |= (k ? 1u : 0u) << (8 * (e & 3));
+      if (per_head && k) {
+        if (row != run_row) {
+          if (run) atomicAdd(&cnt[run_row], run);
+          run_row = row;
+          run = 0;
+        }
+        ++run;
+      }
+    }
+    if (++t == N) {
+      t = 0;
+      ++row;
+    }
   }
-  __shared__ uint32_t red[kThreads / 32];
-  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cnt;
+  if (base + kPerThread <= n) {
+    *reinterpret_cast<uint4 *>(keep + base) = make_uint4(bytes[0], bytes[1], bytes[2], bytes[3]);
+  } else {
+    for (int e = 0; base + e < n; ++e) keep[base + e] = (bytes[e >> 2] >> (8 * (e & 3))) & 1u;
+  }
+  // append the candidates in index order: one atomic per CTA
+  __shared__ uint32_t wsum[kThreads / 32 + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t mine = __popc(cbits);
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  if (per_head && run) atomicAdd(&cnt[run_row], run);
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t s = 0;
-    for (int w = 0; w < kThreads / 32; ++w) s += red[w];
-    tiecnt[blockIdx.x] = s;
+    uint32_t tot = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const uint32_t v = wsum[w];
+      wsum[w] = tot;
+      tot += v;
+    }
+    wsum[kThreads / 32] = tot ? atomicAdd(&st->n_cand, tot) : 0u;
   }
+  __syncthreads();
+  uint32_t pos = wsum[kThreads / 32] + wsum[warp] + incl - mine;
+  for (uint32_t bits = cbits; bits; bits &= bits - 1) {  // scores re-read: L1 hits
+    const int i = base + __ffs(bits) - 1;
+    cand[pos] = static_cast<uint32_t>(i);
+    ckey[pos++] = score_key(__ldg(scores + i));
+  }
+  if (per_head) {
+    for (int i = threadIdx.x; i < n_rows; i += kThreads)
+      if (cnt[i]) atomicAdd(per_head + row0 + i, cnt[i]);
+  }
+}
+
+// Candidate passes.  Each warp takes 32 x kCandPer consecutive entries of the
+// candidate list (index and key) per step; every lane runs every step, lanes
+// past the end carry no candidate.
+// Counts go through warp-aggregated atomics: the lanes that share a target
+// (a bin, a chunk, a row) elect one to add their number, which keeps heavily
+// tied scores from serializing on one address.
+constexpr int kCandPer = 4;
+
+__device__ __forceinline__ void warp_add(uint32_t *addr_base, int slot, bool on, uint32_t n = 1) {
+  const unsigned act = __ballot_sync(0xffffffffu, on);
+  if (!on) return;
+  const unsigned peers = __match_any_sync(act, slot);
+  if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(addr_base + slot, n * __popc(peers));
+}
+
+template <typename F>
+__device__ __forceinline__ void for_candidates(const uint32_t *__restrict__ cand,
+                                               const uint32_t *__restrict__ ckey, uint32_t nc,
+                                               F &&f) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t warps = gridDim.x * (kThreads / 32);
+  const uint32_t step = warps * 32 * kCandPer;
+  for (uint32_t b0 = (blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * 32 * kCandPer;
+       b0 < nc; b0 += step) {
+    uint32_t idx[kCandPer], key[kCandPer];
+#pragma unroll
+    for (int u = 0; u < kCandPer; ++u) {
+      const uint32_t i = b0 + u * 32 + lane;
+      idx[u] = i < nc ? __ldg(cand + i) : 0xFFFFFFFFu;
+      key[u] = i < nc ? __ldg(ckey + i) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kCandPer; ++u) f(b0 + u * 32 + lane < nc, idx[u], key[u]);
+  }
+}
+
+// Histogram of a later digit over the candidates whose decided bits match:
+// level 2, bits 10-20 of every candidate; level 3, bits 0-9 of those whose
+// top 22 bits match.
+template <int LEVEL>
+__global__ void __launch_bounds__(kThreads)
+    topm_cand_hist_kernel(const uint32_t *__restrict__ cand, const uint32_t *__restrict__ ckey,
+                          const TopmState *__restrict__ st, uint32_t *__restrict__ hist) {
+  constexpr int BINS = LEVEL == 2 ? kBins2 : kBins3;
+  __shared__ uint32_t h[BINS];
+  for (int i = threadIdx.x; i < BINS; i += kThreads) h[i] = 0;
+  __syncthreads();
+  const uint32_t nc = st->n_cand, hi = st->prefix >> kShift2;
+  for_candidates(cand, ckey, nc, [&](bool valid, uint32_t, uint32_t k) {
+    if (LEVEL == 2)
+      warp_add(h, static_cast<int>((k >> kShift2) & (kBins2 - 1)), valid);
+    else
+      warp_add(h, static_cast<int>(k & (kBins3 - 1)), valid && (k >> kShift2) == hi);
+  });
+  __syncthreads();
+  for (int i = threadIdx.x; i < BINS; i += kThreads)
+    if (h[i]) atomicAdd(&hist[i], h[i]);
+}
+
+// Candidates whose key equals S*, per chunk of kChunk elements of the array.
+__global__ void __launch_bounds__(kThreads)
+    topm_cand_tie_kernel(const uint32_t *__restrict__ cand, const uint32_t *__restrict__ ckey,
+                         const TopmState *__restrict__ st, uint32_t *__restrict__ tiecnt) {
+  const uint32_t skey = st->prefix;
+  for_candidates(cand, ckey, st->n_cand, [&](bool valid, uint32_t idx, uint32_t k) {
+    warp_add(tiecnt, static_cast<int>(idx / kChunk), valid && k == skey);
+  });
+}
+
+// The kept candidates: (key, index) <= (S*, idx*).
+__global__ void __launch_bounds__(kThreads)
+    topm_cand_keep_kernel(const uint32_t *__restrict__ cand, const uint32_t *__restrict__ ckey,
+                          const TopmState *__restrict__ st, int N, uint8_t *__restrict__ keep,
+                          int32_t *__restrict__ per_head) {
+  const uint32_t skey = st->prefix, istar = st->idx_star;
+  for_candidates(cand, ckey, st->n_cand, [&](bool valid, uint32_t idx, uint32_t k) {
+    const bool kept = valid && (k < skey || (k == skey && idx <= istar));
+    if (kept) keep[idx] = 1;
+    if (per_head)
+      warp_add(reinterpret_cast<uint32_t *>(per_head),
+               static_cast<int>(idx / static_cast<uint32_t>(N)), kept);
+  });
 }
 
 // One CTA of 1024 threads: the chunk holding the k_rem-th tie, from an
@@ -228,15 +397,13 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// The keep mask.  mode 0: only the current positions; 1: every element;
-// 2: candidates with (key, index) <= (S*, idx*).  Kept rows per (layer,
-// head) are summed in shared memory, then added once per CTA.
+// The keep mask when the budget decides it alone.  all = false: only the
+// current positions; true: every element.  Kept rows per (layer, head) are
+// summed in shared memory, then added once per CTA.
 __global__ void __launch_bounds__(kThreads)
-    topm_mask_kernel(const float *__restrict__ scores, int n, int N, int current,
-                     const TopmState *__restrict__ st, int mode, uint8_t *__restrict__ keep,
+    topm_mask_kernel(int n, int N, int current, bool all, uint8_t *__restrict__ keep,
                      int32_t *__restrict__ per_head) {
   __shared__ int cnt[kChunk + 2];  // rows of this chunk, relative to its first
-  const uint32_t skey = st->prefix, istar = st->idx_star;
   const int cbase = blockIdx.x * kChunk;
   const int row0 = static_cast<int>(static_cast<unsigned>(cbase) / static_cast<unsigned>(N));
   const int cend = min(n, cbase + kChunk);
@@ -247,8 +414,6 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
   }
   const int base = cbase + threadIdx.x * kPerThread;
-  float sc[kPerThread];
-  load_run(scores, n, base, sc);
   int t = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
   int row = static_cast<int>(static_cast<unsigned>(base) / static_cast<unsigned>(N)) - row0;
   int run_row = -1, run = 0;  // kept count of the current (layer, head) run
@@ -256,10 +421,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int e = 0; e < kPerThread; ++e) {
     if (base + e < n) {
-      const uint32_t key = score_key(sc[e]);
-      const bool k = t == current || mode == 1 ||
-                     (mode == 2 && (key < skey ||
-                                    (key == skey && static_cast<uint32_t>(base + e) <= istar)));
+      const bool k = all || t == current;
       bytes[e >> 2] |= (k ? 1u : 0u) << (8 * (e & 3));
       if (per_head && k) {
         if (row != run_row) {
@@ -297,10 +459,15 @@ using namespace pa;
 
 extern "C" {
 
+// Workspace: the three histograms, the state, the per-chunk tie counts, then
+// the candidate list (an index and a key per element at most), 16-byte
+// aligned.
 size_t pa_topm_workspace_size(int n_layers, int n_heads, int n_tokens) {
   if (n_layers <= 0 || n_heads <= 0 || n_tokens <= 0) return 0;
   const int64_t n = static_cast<int64_t>(n_layers) * n_heads * n_tokens;
-  return 256 * sizeof(uint32_t) + sizeof(TopmState) + topm_chunks(n) * sizeof(uint32_t);
+  const size_t head = (kBins1 + kBins2 + kBins3) * sizeof(uint32_t) + sizeof(TopmState) +
+                      topm_chunks(n) * sizeof(uint32_t);
+  return ((head + 15) & ~size_t(15)) + 2 * static_cast<size_t>(n) * sizeof(uint32_t);
 }
 
 int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens, int current,
@@ -319,37 +486,52 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
        reinterpret_cast<uintptr_t>(keep)) & 15)
     return PA_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint32_t *hist = static_cast<uint32_t *>(workspace);
-  TopmState *st = reinterpret_cast<TopmState *>(hist + 256);
+  uint32_t *hist1 = static_cast<uint32_t *>(workspace);
+  uint32_t *hist2 = hist1 + kBins1, *hist3 = hist2 + kBins2;
+  TopmState *st = reinterpret_cast<TopmState *>(hist3 + kBins3);
   uint32_t *tiecnt = reinterpret_cast<uint32_t *>(st + 1);
   const int n_chunks = static_cast<int>(topm_chunks(n));
+  const size_t head = reinterpret_cast<uint8_t *>(tiecnt + n_chunks) -
+                      static_cast<uint8_t *>(workspace);
+  uint32_t *cand =
+      reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + ((head + 15) & ~size_t(15)));
+  uint32_t *ckey = cand + n;
   const int64_t n_cand = static_cast<int64_t>(n_layers) * n_heads * (n_tokens - 1);
   const int64_t k = budget - static_cast<int64_t>(n_layers) * n_heads;  // candidates kept
   const int mode = k <= 0 ? 0 : (k >= n_cand ? 1 : 2);
   if (kept_per_head &&
       cudaMemsetAsync(kept_per_head, 0, sizeof(int32_t) * n_layers * n_heads, s) != cudaSuccess)
     return PA_ERR_CUDA;
-  topm_init_kernel<<<1, 256, 0, s>>>(hist, st, mode == 2 ? static_cast<uint32_t>(k) : 0u);
-  if (mode == 2) {
-    int sms = 148;
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = n_chunks < sms * 4 ? n_chunks : sms * 4;
-    const int ni = static_cast<int>(n);
-    for (int d = 0; d < 4; ++d) {
-      const int shift = 24 - 8 * d;
-      topm_hist_kernel<<<grid, kThreads, 0, s>>>(scores, ni, n_tokens, current, hist, st,
-                                                 shift);
-      topm_pick_kernel<<<1, kThreads, 0, s>>>(hist, st, shift);
-    }
-    topm_tiecount_kernel<<<n_chunks, kThreads, 0, s>>>(scores, ni, n_tokens, current, st,
-                                                       tiecnt);
-    topm_scan_kernel<<<1, 1024, 0, s>>>(tiecnt, n_chunks, st);
-    topm_tiefind_kernel<<<1, kThreads, 0, s>>>(scores, ni, n_tokens, current, st);
+  const int ni = static_cast<int>(n);
+  if (mode != 2) {
+    topm_mask_kernel<<<n_chunks, kThreads, 0, s>>>(ni, n_tokens, current, mode == 1, keep,
+                                                   kept_per_head);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
-  topm_mask_kernel<<<n_chunks, kThreads, 0, s>>>(scores, static_cast<int>(n), n_tokens,
-                                                 current, st, mode, keep, kept_per_head);
+  int sms = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int n_zero = kBins1 + kBins2 + kBins3;  // the state follows, set apart
+  topm_init_kernel<<<(n_zero + kThreads - 1) / kThreads, kThreads, 0, s>>>(
+      hist1, n_zero, st, static_cast<uint32_t>(k));
+  if (cudaMemsetAsync(tiecnt, 0, sizeof(uint32_t) * n_chunks, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  const int grid = n_chunks < sms * 4 ? n_chunks : sms * 4;
+  const int cgrid = sms * 4;  // candidate passes: grid-stride over the list
+  topm_hist1_kernel<<<grid, kThreads, 0, s>>>(scores, ni, n_tokens, current, hist1);
+  topm_pick_kernel<kBins1><<<1, 1024, 0, s>>>(hist1, st, kShift1);
+  topm_split_kernel<<<n_chunks, kThreads, 0, s>>>(scores, ni, n_tokens, current, st, keep,
+                                                  kept_per_head, cand, ckey);
+  topm_cand_hist_kernel<2><<<cgrid, kThreads, 0, s>>>(cand, ckey, st, hist2);
+  topm_pick_kernel<kBins2><<<1, 1024, 0, s>>>(hist2, st, kShift2);
+  topm_cand_hist_kernel<3><<<cgrid, kThreads, 0, s>>>(cand, ckey, st, hist3);
+  topm_pick_kernel<kBins3><<<1, 1024, 0, s>>>(hist3, st, 0);
+  topm_cand_tie_kernel<<<cgrid, kThreads, 0, s>>>(cand, ckey, st, tiecnt);
+  topm_scan_kernel<<<1, 1024, 0, s>>>(tiecnt, n_chunks, st);
+  topm_tiefind_kernel<<<1, kThreads, 0, s>>>(scores, ni, n_tokens, current, st);
+  topm_cand_keep_kernel<<<cgrid, kThreads, 0, s>>>(cand, ckey, st, n_tokens, keep,
+                                                   kept_per_head);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

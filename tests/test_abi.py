@@ -203,12 +203,13 @@ def test_topm_arguments(L):
     P = FAKE
     ws = L.pa_topm_workspace_size(32, 32, 32768)
     n = 32 * 32 * 32768
-    assert ws == 256 * 4 + 32 + -(-n // 4096) * 4
+    head = (2048 + 2048 + 1024) * 4 + 32 + -(-n // 4096) * 4  # histograms, state, tie counts
+    assert ws == -(-head // 16) * 16 + 8 * n                   # + a candidate (index, key) per element
     assert L.pa_topm_workspace_size(0, 1, 1) == 0
     r = L.pa_topm_retain
     assert r(None, 2, 2, 8, 0, 5, P, None, P, ws, None) == -1
     assert r(P, 2, 2, 8, 8, 5, P, None, P, ws, None) == -5     # current outside
     assert r(P, 2, 2, 8, 0, -1, P, None, P, ws, None) == -5    # negative budget
     assert r(P, 2, 2, 8, 0, 5, P, None, P, 16, None) == -7     # workspace too small
-    assert r(P + 4, 2, 2, 8, 0, 5, P, None, P, 4096, None) == -8
+    assert r(P + 4, 2, 2, 8, 0, 5, P, None, P, 1 << 20, None) == -8
     assert r(P, 1 << 16, 1 << 16, 2, 0, 5, P, None, P, 1 << 40, None) == -5

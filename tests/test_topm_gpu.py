@@ -74,3 +74,19 @@ def test_topm_full_size():
     got = keep.cpu().numpy().astype(bool)
     assert int(got.sum()) == budget and np.array_equal(got, want)
     assert np.array_equal(per_head.cpu().numpy(), want.sum(axis=2))
+
+
+def test_topm_all_scores_equal():
+    """Every element ties: the whole array is one candidate bucket and the
+    index order alone decides (lowest (l, h, t) first)."""
+    L, H, N = 3, 4, 5000
+    s = np.full((L, H, N), 1.5, dtype=np.float32)
+    dev = torch.from_numpy(s).cuda()
+    n = L * H * N
+    for budget in (L * H + 1, n // 3, n - 2):
+        keep, per_head = pa.topm_retain(dev, 7, budget)
+        torch.cuda.synchronize()
+        want = oracle.topm_retain(s, 7, budget)
+        assert np.array_equal(keep.cpu().numpy().astype(bool), want), budget
+        assert np.array_equal(per_head.cpu().numpy(), want.sum(axis=2)), budget
+    assert pa.pa_last_device_error() == 0

@@ -58,12 +58,19 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return ~u;                                        // descending
 }
 
-// Zeroes the three histograms and the per-chunk tie counts, sets the state.
+// Zeroes the three histograms, the per-chunk tie counts and the kept-row
+// counts, sets the state.
 __global__ void __launch_bounds__(kThreads)
-    topm_init_kernel(uint32_t *__restrict__ hist, int n_zero, TopmState *__restrict__ st,
-                     uint32_t k) {
-  for (int i = blockIdx.x * kThreads + threadIdx.x; i < n_zero; i += gridDim.x * kThreads)
-    hist[i] = 0;
+    topm_init_kernel(uint32_t *__restrict__ hist, int n_hist, uint32_t *__restrict__ tiecnt,
+                     int n_chunks, int32_t *__restrict__ per_head, int n_rows,
+                     TopmState *__restrict__ st, uint32_t k) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
+  const int stride = gridDim.x * kThreads;
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < n_hist; i += stride) hist[i] = 0;
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < n_chunks; i += stride) tiecnt[i] = 0;
+  if (per_head)
+    for (int i = blockIdx.x * kThreads + threadIdx.x; i < n_rows; i += stride) per_head[i] = 0;
   if (blockIdx.x == 0 && threadIdx.x == 0) *st = TopmState{0u, 0u, k, 0u, 0u, 0u, 0u, 0u};
 }
 
@@ -92,16 +99,24 @@ __device__ __forceinline__ void load_run(const float *__restrict__ scores, int n
 __global__ void __launch_bounds__(kThreads)
     topm_hist1_kernel(const float *__restrict__ scores, int n, int N, int current,
                       uint32_t *__restrict__ hist) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
   constexpr int kCopies = 4;
   __shared__ uint32_t h[kCopies][kBins1];
   for (int i = threadIdx.x; i < kCopies * kBins1; i += kThreads) h[i / kBins1][i % kBins1] = 0;
   __syncthreads();
   uint32_t *mine = h[(threadIdx.x >> 5) & (kCopies - 1)];
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kChunk;
-  for (int64_t cbase = static_cast<int64_t>(blockIdx.x) * kChunk; cbase < n; cbase += stride) {
+  float nx[kPerThread];  // the next chunk's run, loaded while this one is counted
+  int64_t cbase = static_cast<int64_t>(blockIdx.x) * kChunk;
+  if (cbase < n) load_run(scores, n, static_cast<int>(cbase) + threadIdx.x * kPerThread, nx);
+  for (; cbase < n; cbase += stride) {
     const int base = static_cast<int>(cbase) + threadIdx.x * kPerThread;
     float sc[kPerThread];
-    load_run(scores, n, base, sc);
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) sc[e] = nx[e];
+    if (cbase + stride < n)
+      load_run(scores, n, static_cast<int>(cbase + stride) + threadIdx.x * kPerThread, nx);
     int t = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
 #pragma unroll
     for (int e = 0; e < kPerThread; ++e) {
@@ -123,6 +138,8 @@ __global__ void __launch_bounds__(kThreads)
 template <int BINS>
 __global__ void __launch_bounds__(1024)
     topm_pick_kernel(uint32_t *__restrict__ hist, TopmState *__restrict__ st, int shift) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
   constexpr int kPer = BINS / 1024;
   __shared__ uint32_t c[1024];
   const int t = threadIdx.x;
@@ -166,6 +183,8 @@ __global__ void __launch_bounds__(kThreads, 8)
                       TopmState *__restrict__ st, uint8_t *__restrict__ keep,
                       int32_t *__restrict__ per_head, uint32_t *__restrict__ cand,
                       uint32_t *__restrict__ ckey) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
   __shared__ int cnt[kChunk + 2];  // rows of this chunk, relative to its first
   const uint32_t b1 = st->prefix >> kShift1;
   const int cbase = blockIdx.x * kChunk;
@@ -289,6 +308,8 @@ template <int LEVEL>
 __global__ void __launch_bounds__(kThreads)
     topm_cand_hist_kernel(const uint32_t *__restrict__ cand, const uint32_t *__restrict__ ckey,
                           const TopmState *__restrict__ st, uint32_t *__restrict__ hist) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
   constexpr int BINS = LEVEL == 2 ? kBins2 : kBins3;
   __shared__ uint32_t h[BINS];
   for (int i = threadIdx.x; i < BINS; i += kThreads) h[i] = 0;
@@ -309,6 +330,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     topm_cand_tie_kernel(const uint32_t *__restrict__ cand, const uint32_t *__restrict__ ckey,
                          const TopmState *__restrict__ st, uint32_t *__restrict__ tiecnt) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
   const uint32_t skey = st->prefix;
   for_candidates(cand, ckey, st->n_cand, [&](bool valid, uint32_t idx, uint32_t k) {
     warp_add(tiecnt, static_cast<int>(idx / kChunk), valid && k == skey);
@@ -320,6 +343,8 @@ __global__ void __launch_bounds__(kThreads)
     topm_cand_keep_kernel(const uint32_t *__restrict__ cand, const uint32_t *__restrict__ ckey,
                           const TopmState *__restrict__ st, int N, uint8_t *__restrict__ keep,
                           int32_t *__restrict__ per_head) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
   const uint32_t skey = st->prefix, istar = st->idx_star;
   for_candidates(cand, ckey, st->n_cand, [&](bool valid, uint32_t idx, uint32_t k) {
     const bool kept = valid && (k < skey || (k == skey && idx <= istar));
@@ -335,6 +360,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(1024)
     topm_scan_kernel(const uint32_t *__restrict__ tiecnt, int n_chunks,
                      TopmState *__restrict__ st) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
   __shared__ uint32_t c[1024];
   const int per = (n_chunks + 1023) / 1024;
   const int lo = threadIdx.x * per, hi = min(n_chunks, lo + per);
@@ -368,6 +395,8 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(kThreads)
     topm_tiefind_kernel(const float *__restrict__ scores, int n, int N, int current,
                         TopmState *__restrict__ st) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
   const uint32_t skey = st->prefix, want = st->tie_rank;
   const int base = static_cast<int>(st->tie_chunk) * kChunk + threadIdx.x * kPerThread;
   float sc[kPerThread];
@@ -403,6 +432,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     topm_mask_kernel(int n, int N, int current, bool all, uint8_t *__restrict__ keep,
                      int32_t *__restrict__ per_head) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
   __shared__ int cnt[kChunk + 2];  // rows of this chunk, relative to its first
   const int cbase = blockIdx.x * kChunk;
   const int row0 = static_cast<int>(static_cast<unsigned>(cbase) / static_cast<unsigned>(N));
@@ -499,11 +530,11 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
   const int64_t n_cand = static_cast<int64_t>(n_layers) * n_heads * (n_tokens - 1);
   const int64_t k = budget - static_cast<int64_t>(n_layers) * n_heads;  // candidates kept
   const int mode = k <= 0 ? 0 : (k >= n_cand ? 1 : 2);
-  if (kept_per_head &&
-      cudaMemsetAsync(kept_per_head, 0, sizeof(int32_t) * n_layers * n_heads, s) != cudaSuccess)
-    return PA_ERR_CUDA;
   const int ni = static_cast<int>(n);
   if (mode != 2) {
+    if (kept_per_head &&
+        cudaMemsetAsync(kept_per_head, 0, sizeof(int32_t) * n_layers * n_heads, s) != cudaSuccess)
+      return PA_ERR_CUDA;
     topm_mask_kernel<<<n_chunks, kThreads, 0, s>>>(ni, n_tokens, current, mode == 1, keep,
                                                    kept_per_head);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -513,26 +544,35 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int n_zero = kBins1 + kBins2 + kBins3;  // the state follows, set apart
-  topm_init_kernel<<<(n_zero + kThreads - 1) / kThreads, kThreads, 0, s>>>(
-      hist1, n_zero, st, static_cast<uint32_t>(k));
-  if (cudaMemsetAsync(tiecnt, 0, sizeof(uint32_t) * n_chunks, s) != cudaSuccess)
-    return PA_ERR_CUDA;
+  // Every kernel waits for its predecessor at entry (programmatic dependent
+  // launch: only the launch latency overlaps).
   const int grid = n_chunks < sms * 4 ? n_chunks : sms * 4;
   const int cgrid = sms * 4;  // candidate passes: grid-stride over the list
-  topm_hist1_kernel<<<grid, kThreads, 0, s>>>(scores, ni, n_tokens, current, hist1);
-  topm_pick_kernel<kBins1><<<1, 1024, 0, s>>>(hist1, st, kShift1);
-  topm_split_kernel<<<n_chunks, kThreads, 0, s>>>(scores, ni, n_tokens, current, st, keep,
-                                                  kept_per_head, cand, ckey);
-  topm_cand_hist_kernel<2><<<cgrid, kThreads, 0, s>>>(cand, ckey, st, hist2);
-  topm_pick_kernel<kBins2><<<1, 1024, 0, s>>>(hist2, st, kShift2);
-  topm_cand_hist_kernel<3><<<cgrid, kThreads, 0, s>>>(cand, ckey, st, hist3);
-  topm_pick_kernel<kBins3><<<1, 1024, 0, s>>>(hist3, st, 0);
-  topm_cand_tie_kernel<<<cgrid, kThreads, 0, s>>>(cand, ckey, st, tiecnt);
-  topm_scan_kernel<<<1, 1024, 0, s>>>(tiecnt, n_chunks, st);
-  topm_tiefind_kernel<<<1, kThreads, 0, s>>>(scores, ni, n_tokens, current, st);
-  topm_cand_keep_kernel<<<cgrid, kThreads, 0, s>>>(cand, ckey, st, n_tokens, keep,
-                                                   kept_per_head);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const dim3 T(kThreads), one(1), T1k(1024);
+  const int n_rows = n_layers * n_heads;
+  cudaError_t e = launch_pdl(topm_init_kernel, dim3(sms), T, 0, s, hist1, n_zero, tiecnt,
+                             n_chunks, kept_per_head, n_rows, st, static_cast<uint32_t>(k));
+  if (e == cudaSuccess)
+    e = launch_pdl(topm_hist1_kernel, dim3(grid), T, 0, s, scores, ni, n_tokens, current, hist1);
+  if (e == cudaSuccess) e = launch_pdl(topm_pick_kernel<kBins1>, one, T1k, 0, s, hist1, st, kShift1);
+  if (e == cudaSuccess)
+    e = launch_pdl(topm_split_kernel, dim3(n_chunks), T, 0, s, scores, ni, n_tokens, current, st,
+                   keep, kept_per_head, cand, ckey);
+  if (e == cudaSuccess)
+    e = launch_pdl(topm_cand_hist_kernel<2>, dim3(cgrid), T, 0, s, cand, ckey, st, hist2);
+  if (e == cudaSuccess) e = launch_pdl(topm_pick_kernel<kBins2>, one, T1k, 0, s, hist2, st, kShift2);
+  if (e == cudaSuccess)
+    e = launch_pdl(topm_cand_hist_kernel<3>, dim3(cgrid), T, 0, s, cand, ckey, st, hist3);
+  if (e == cudaSuccess) e = launch_pdl(topm_pick_kernel<kBins3>, one, T1k, 0, s, hist3, st, 0);
+  if (e == cudaSuccess)
+    e = launch_pdl(topm_cand_tie_kernel, dim3(cgrid), T, 0, s, cand, ckey, st, tiecnt);
+  if (e == cudaSuccess) e = launch_pdl(topm_scan_kernel, one, T1k, 0, s, tiecnt, n_chunks, st);
+  if (e == cudaSuccess)
+    e = launch_pdl(topm_tiefind_kernel, one, T, 0, s, scores, ni, n_tokens, current, st);
+  if (e == cudaSuccess)
+    e = launch_pdl(topm_cand_keep_kernel, dim3(cgrid), T, 0, s, cand, ckey, st, n_tokens, keep,
+                   kept_per_head);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // extern "C"

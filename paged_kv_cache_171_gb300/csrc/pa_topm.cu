@@ -117,12 +117,25 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = 0; e < kPerThread; ++e) sc[e] = nx[e];
     if (cbase + stride < n)
       load_run(scores, n, static_cast<int>(cbase + stride) + threadIdx.x * kPerThread, nx);
-    int t = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
+    const int t0 = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
+    uint32_t skip;  // elements that are a current position or past the array
+    if (base + kPerThread <= n && N >= kPerThread) {
+      skip = 0;
+      if (current >= t0 && current - t0 < kPerThread) skip |= 1u << (current - t0);
+      const unsigned e1 = static_cast<unsigned>(N - t0) + static_cast<unsigned>(current);
+      if (e1 < static_cast<unsigned>(kPerThread)) skip |= 1u << e1;
+    } else {
+      skip = 0;
+      int t = t0;
 #pragma unroll
-    for (int e = 0; e < kPerThread; ++e) {
-      if (base + e < n && t != current) atomicAdd(&mine[score_key(sc[e]) >> kShift1], 1u);
-      if (++t == N) t = 0;
+      for (int e = 0; e < kPerThread; ++e) {
+        if (base + e >= n || t == current) skip |= 1u << e;
+        if (++t == N) t = 0;
+      }
     }
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e)
+      if (!(skip >> e & 1u)) atomicAdd(&mine[score_key(sc[e]) >> kShift1], 1u);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < kBins1; i += kThreads) {
@@ -199,18 +212,48 @@ __global__ void __launch_bounds__(kThreads, 8)
   const int base = cbase + threadIdx.x * kPerThread;
   float sc[kPerThread];
   load_run(scores, n, base, sc);
-  int t = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
-  int row = static_cast<int>(static_cast<unsigned>(base) / static_cast<unsigned>(N)) - row0;
-  int run_row = -1, run = 0;  // kept count of the current (layer, head) run
-  uint32_t bytes[kPerThread / 4] = {0u, 0u, 0u, 0u};
-  uint32_t cbits = 0;  // bit e: element base + e is a candidate
+  const int t0 = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
+  const int r0 = static_cast<int>(static_cast<unsigned>(base) / static_cast<unsigned>(N)) - row0;
+  uint32_t kbits = 0, cbits = 0;  // bit e: element base + e is kept / a candidate
+  if (base + kPerThread <= n && N >= kPerThread) {
+    // Whole run, at most one row boundary (at element N - t0 when t0 + 16 > N):
+    // decisions as bit masks, no per-element branches.
+    uint32_t cur = 0;  // the current positions among the 16
+    if (current >= t0 && current - t0 < kPerThread) cur |= 1u << (current - t0);
+    const unsigned e1 = static_cast<unsigned>(N - t0) + static_cast<unsigned>(current);
+    if (e1 < static_cast<unsigned>(kPerThread)) cur |= 1u << e1;  // in the next row
 #pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    if (base + e < n) {
+    for (int e = 0; e < kPerThread; ++e) {
+      const uint32_t bk = score_key(sc[e]) >> kShift1;
+      kbits |= static_cast<uint32_t>(bk < b1) << e;
+      cbits |= static_cast<uint32_t>(bk == b1) << e;
+    }
+    kbits |= cur;
+    cbits &= ~cur;
+    uint4 w;  // bit e of kbits -> byte e
+    w.x = ((kbits & 15u) * 0x00204081u) & 0x01010101u;
+    w.y = (((kbits >> 4) & 15u) * 0x00204081u) & 0x01010101u;
+    w.z = (((kbits >> 8) & 15u) * 0x00204081u) & 0x01010101u;
+    w.w = (((kbits >> 12) & 15u) * 0x00204081u) & 0x01010101u;
+    *reinterpret_cast<uint4 *>(keep + base) = w;
+    if (per_head) {
+      const int split = N - t0 < kPerThread ? N - t0 : kPerThread;  // elements in row r0
+      const uint32_t lo = kbits & ((1u << split) - 1u), hi = kbits >> split;
+      if (lo) atomicAdd(&cnt[r0], __popc(lo));
+      if (hi) atomicAdd(&cnt[r0 + 1], __popc(hi));
+    }
+  } else {
+    // The array's ragged end, or rows shorter than a run: element by element.
+    int t = t0, row = r0;
+    int run_row = -1, run = 0;  // kept count of the current (layer, head) run
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) {
+      if (base + e >= n) break;
       const uint32_t bk = score_key(sc[e]) >> kShift1;
       const bool k = t == current || bk < b1;
       if (t != current && bk == b1) cbits |= 1u << e;
-      bytes[e >> 2] |= (k ? 1u : 0u) << (8 * (e & 3));
+      kbits |= static_cast<uint32_t>(k) << e;
+      keep[base + e] = k ? 1u : 0u;
       if (per_head && k) {
         if (row != run_row) {
           if (run) atomicAdd(&cnt[run_row], run);
@@ -219,16 +262,12 @@ __global__ void __launch_bounds__(kThreads, 8)
         }
         ++run;
       }
+      if (++t == N) {
+        t = 0;
+        ++row;
+      }
     }
-    if (++t == N) {
-      t = 0;
-      ++row;
-    }
-  }
-  if (base + kPerThread <= n) {
-    *reinterpret_cast<uint4 *>(keep + base) = make_uint4(bytes[0], bytes[1], bytes[2], bytes[3]);
-  } else {
-    for (int e = 0; base + e < n; ++e) keep[base + e] = (bytes[e >> 2] >> (8 * (e & 3))) & 1u;
+    if (per_head && run) atomicAdd(&cnt[run_row], run);
   }
   // append the candidates in index order: one atomic per CTA
   __shared__ uint32_t wsum[kThreads / 32 + 1];
@@ -241,7 +280,6 @@ __global__ void __launch_bounds__(kThreads, 8)
     if (lane >= o) incl += u;
   }
   if (lane == 31) wsum[warp] = incl;
-  if (per_head && run) atomicAdd(&cnt[run_row], run);
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t tot = 0;

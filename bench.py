@@ -858,7 +858,8 @@ def ncu_case(args):
             pa.pa_copy_pages(kc, vc, src, dst, 4096, 8, 128, 16, 8192, pa.BF16)
     else:
         name = {"decode": HEADLINE, "decode_gqa8": "gqa8_b4_ctx32k",
-                "decode_gqa4": "gqa4_b64_ragged"}[args.ncu_case]
+                "decode_gqa4": "gqa4_b64_ragged", "decode_mha_small": "mha_b1_ctx512"}[
+                    args.ncu_case]
         over = {"layers": 1, "pool_pages": None}
         case = workloads.config_case(name, device="cuda", **over)
         part = workloads.CONFIGS[name].get("partition_tokens", 0)
@@ -878,9 +879,9 @@ def main():
     ap.add_argument("--only-headline", action="store_true",
                     help="skip the other workloads (ragged GQA, 32k split-K, prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["decode", "decode_gqa8", "decode_gqa4", "verify",
-                                           "window", "topm", "copy_pages",
-                                           "prefill"],
+    ap.add_argument("--ncu-case", choices=["decode", "decode_gqa8", "decode_gqa4",
+                                           "decode_mha_small", "verify", "window", "topm",
+                                           "copy_pages", "prefill"],
                     help="run a small launch sequence for an ncu capture and exit")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -159,7 +159,8 @@ int sm_count() {
 // partition count.  Automatic mode, with R = resident CTAs (2 per SM) and
 // I = batch * kv heads * head tiles (CTAs of a single pass):
 //   I <  3R/4: cut sequences into about R / I equal partitions, so that one
-//              wave of CTAs keeps enough copies in flight;
+//              wave of CTAs keeps enough copies in flight, of at most 256
+//              pages each;
 //   I <  R   : a single pass (one wave, no merge);
 //   I >= R   : cut into 4 partitions of >= 32 pages, so that one long
 //              sequence of a ragged batch cannot make a tail of its own.
@@ -177,6 +178,7 @@ int decode_plan(int batch, int n_q_heads, int n_kv_heads, int max_blocks,
       const int64_t want = resident / items > 1 ? resident / items : 1;
       int64_t per = (max_blocks + want - 1) / want;
       if (per < 16) per = 16;
+      if (per > 256) per = 256;  // longer ranges leave a slow tail (measured at 32k)
       pp = static_cast<int>(per);
     } else if (items < resident) {
       pp = 0;

@@ -408,6 +408,17 @@ int pa_decode_static_workspace(const void *q, const void *k_cache,
  */
 int pa_last_device_error(pa_stream_t stream);
 
+/*
+ * pa_selftest_wait_timeout -- exercise the failure path of the kernels'
+ * bounded waits.  The pages have no counterpart: every copy or hand-off a pa
+ * kernel waits for is waited on for at most 2 s, after which the kernel
+ * records PA_ERR_TIMEOUT in the device status word and leaves without
+ * faulting.  This launches one warp that waits on a barrier phase nothing
+ * completes, so the next pa_last_device_error() returns PA_ERR_TIMEOUT after
+ * about 2 s, and later calls run normally.  Asynchronous on `stream`.
+ */
+int pa_selftest_wait_timeout(pa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,8 @@ __all__ = [
     "pa_pool_create", "pa_pool_destroy", "pa_pool_free_pages", "pa_pool_refcount",
     "pa_pool_alloc", "pa_pool_share", "pa_pool_release", "pa_pool_prepare_append",
     "pa_copy_pages", "pa_topm_retain", "pa_topm_workspace_size", "topm_retain",
-    "pa_last_device_error", "pa_strerror", "decode", "prefill", "prefill_split",
+    "pa_last_device_error", "pa_selftest_wait_timeout", "pa_strerror", "decode", "prefill",
+    "prefill_split",
     "append_kv",
 ]
 
@@ -103,6 +104,8 @@ def lib():
         L.pa_decode_static_workspace.restype = I
         L.pa_last_device_error.argtypes = [P]
         L.pa_last_device_error.restype = I
+        L.pa_selftest_wait_timeout.argtypes = [P]
+        L.pa_selftest_wait_timeout.restype = I
         _lib = L
     return _lib
 
@@ -353,6 +356,12 @@ def pa_topm_retain(scores, n_layers, n_heads, n_tokens, current, budget, keep,
 def pa_last_device_error(stream=None) -> int:
     """Synchronises the stream; returns and clears the device status word."""
     return lib().pa_last_device_error(_stream(stream))
+
+
+def pa_selftest_wait_timeout(stream=None):
+    """One warp waits on a barrier phase nothing completes; the bounded wait
+    gives up after 2 s and records PA_ERR_TIMEOUT."""
+    return _check(lib().pa_selftest_wait_timeout(_stream(stream)), "pa_selftest_wait_timeout")
 
 
 # --- tensor-shaped conveniences (allocation by torch, compute by libpa) ------

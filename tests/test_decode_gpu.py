@@ -160,3 +160,23 @@ def test_full_gqa4_b64_ragged_sampled():
 
 def test_full_gqa8_b4_ctx32k_all_rows():
     _full_size_check("gqa8_b4_ctx32k", [0], [0, 1, 2, 3], partition_tokens=512)
+
+
+def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable():
+    """A wait on a barrier phase nothing completes (a copy that never lands)
+    ends after the 2 s limit with PA_ERR_TIMEOUT in the status word; the next
+    call runs normally."""
+    import time
+    t0 = time.monotonic()
+    pa.pa_selftest_wait_timeout()
+    status = pa.pa_last_device_error()
+    dt = time.monotonic() - t0
+    assert status == -13, pa.pa_strerror(status)  # PA_ERR_TIMEOUT
+    assert 1.5 < dt < 30.0, dt
+    assert pa.pa_last_device_error() == 0  # read and cleared
+    kw = dict(layers=1, batch=2, n_q_heads=8, n_kv_heads=8, head_dim=64, page_size=16,
+              ctx=[100, 33], dtype="bf16", seed=99)
+    ref = _oracle(workloads.paged_case(**kw))
+    out = _run_decode(to_device(workloads.paged_case(**kw), "cuda"), partition_tokens=0)
+    assert_close(out.cpu().numpy(), ref, "decode after a timed-out wait")
+    assert pa.pa_last_device_error() == 0

@@ -1,0 +1,116 @@
+"""Seeded random configurations of every entry point against the oracle:
+shapes, group sizes, head dims, dtypes, context mixes (empty, one token,
+page and tile edges, long) and partition sizes drawn at random, sized so the
+oracle finishes in seconds.  Complements the hand-picked cases: it reaches
+combinations of the kernels' modes (single pass / key ranges / warp-owned
+partitions; interleaved and split-row prefill tiles; sink + window spans)
+that nobody listed."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_171_gb300 as pa
+import workloads
+from tests.gpu_support import assert_close, to_device
+
+pytestmark = pytest.mark.gpu
+
+HEADS = [(8, 8), (16, 4), (32, 8), (24, 8), (64, 8), (12, 4), (16, 2), (6, 3)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_171_gb300 import build
+    build.build()
+
+
+def _ctx(rng, n, hi):
+    edges = [0, 1, 15, 16, 17, 127, 128, 129, 511, 512, 513]
+    return [int(rng.choice(edges)) if rng.random() < 0.4 else int(rng.integers(0, hi))
+            for _ in range(n)]
+
+
+def _case(rng, kind, n_new=0, hi=2500):
+    hq, hkv = HEADS[rng.integers(len(HEADS))]
+    kw = dict(layers=1, batch=int(rng.integers(1, 5)), n_q_heads=hq, n_kv_heads=hkv,
+              head_dim=int(rng.choice([64, 128])), page_size=16,
+              dtype=str(rng.choice(["bf16", "fp16"])), seed=int(rng.integers(1 << 30)),
+              extra_pool_pages=3)
+    kw["ctx"] = _ctx(rng, kw["batch"], hi)
+    if kind == "prefill":
+        kw.update(n_new=n_new, kind="prefill")
+    return kw
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_decode(seed):
+    rng = np.random.default_rng(7000 + seed)
+    kw = _case(rng, "decode")
+    cpu = workloads.paged_case(**kw)
+    ref = oracle.decode(cpu.q[0], cpu.k_cache, cpu.v_cache, cpu.block_table[0], cpu.ctx_lens,
+                        cpu.scale, cpu.dtype_code)
+    dev = to_device(workloads.paged_case(**kw), "cuda")
+    part = int(rng.choice([0, 16, 32, 64, 256, 512]))
+    out = pa.decode(dev.q[0], dev.k_cache, dev.v_cache, dev.block_table[0], dev.ctx_lens,
+                    dev.scale, partition_tokens=part)
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), ref, f"decode {kw} part {part}")
+    assert pa.pa_last_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_prefill_and_split(seed):
+    rng = np.random.default_rng(8000 + seed)
+    n_new = int(rng.choice([1, 2, 3, 4, 8, int(rng.integers(1, 200))]))
+    kw = _case(rng, "prefill", n_new=n_new, hi=1500)
+    cpu = workloads.paged_case(**kw)
+    ref = oracle.prefill(cpu.q[0], cpu.k_cache, cpu.v_cache, cpu.block_table[0],
+                         cpu.ctx_lens, cpu.scale, cpu.dtype_code)
+    dev = to_device(workloads.paged_case(**kw), "cuda")
+    out = pa.prefill(dev.q[0], dev.k_cache, dev.v_cache, dev.block_table[0], dev.ctx_lens,
+                     dev.scale)
+    part = int(rng.choice([0, 128, 256, 512]))
+    out_s = pa.prefill_split(dev.q[0], dev.k_cache, dev.v_cache, dev.block_table[0],
+                             dev.ctx_lens, dev.scale, partition_tokens=part)
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), ref, f"prefill {kw}")
+    assert_close(out_s.cpu().numpy(), ref, f"split prefill {kw} part {part}")
+    assert pa.pa_last_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_window(seed):
+    rng = np.random.default_rng(9000 + seed)
+    kw = _case(rng, "decode")
+    sink, window = int(rng.integers(0, 40)), int(rng.choice([0, 1, 16, 100, 500, 2000]))
+    cpu = workloads.paged_case(**kw)
+    ref = oracle.decode_window(cpu.q[0], cpu.k_cache, cpu.v_cache, cpu.block_table[0],
+                               cpu.ctx_lens, cpu.scale, cpu.dtype_code, sink, window)
+    dev = to_device(workloads.paged_case(**kw), "cuda")
+    part = int(rng.choice([0, 16, 64, 256]))
+    out = pa.decode_window(dev.q[0], dev.k_cache, dev.v_cache, dev.block_table[0],
+                           dev.ctx_lens, dev.scale, sink, window, partition_tokens=part)
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), ref, f"window {kw} sink {sink} window {window} part {part}")
+    assert pa.pa_last_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_topm(seed):
+    rng = np.random.default_rng(9500 + seed)
+    L, H, N = int(rng.integers(1, 6)), int(rng.integers(1, 9)), int(rng.integers(1, 3000))
+    grid = rng.choice([0, 1, 4, 16])
+    s = rng.standard_normal((L, H, N)).astype(np.float32)
+    if grid:
+        s = (np.round(s * grid) / grid).astype(np.float32)
+    current = int(rng.integers(0, N))
+    n = L * H * N
+    dev = torch.from_numpy(s).cuda()
+    for budget in (int(rng.integers(0, n + 2)), int(rng.integers(L * H, n + 1))):
+        keep, per_head = pa.topm_retain(dev, current, budget)
+        torch.cuda.synchronize()
+        want = oracle.topm_retain(s, current, budget)
+        assert np.array_equal(keep.cpu().numpy().astype(bool), want), (L, H, N, budget)
+        assert np.array_equal(per_head.cpu().numpy(), want.sum(axis=2)), (L, H, N, budget)
+    assert pa.pa_last_device_error() == 0

@@ -238,7 +238,7 @@ def run_headline(torch, pa, workloads, args, rank, world):
     ms = t0.elapsed_time(t1)
     ms_max = allreduce_max(torch, world, ms)
 
-    # The dominant call (pa_decode: partition kernel + merge) timed on its own
+    # The dominant call (pa_decode) timed on its own
     # stream with events around each call, over the same number of steps.
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
           for _ in range(args.steps)]
@@ -521,7 +521,7 @@ def run_window(torch, pa, workloads, steps, warmup, peaks, sink=4, window=4096):
     res = {"ms_per_step": round(ms, 4), "GB_s": round(gbs, 1),
            "frac_of_hbm_peak": round(gbs / peaks.get("hbm_gbs", 6800.0), 4),
            "sink": sink, "window": window, "context": ctx, "bytes_per_step": nbytes,
-           "kernel": "decode_kernel over the sink + window pages (+ merge when split)",
+           "kernel": "decode_kernel over the sink + window pages (in-kernel merge when split)",
            "l2": "inputs larger than 2x L2, no flush; steps timed back to back"}
     del case, out, ws
     torch.cuda.empty_cache()
@@ -757,7 +757,7 @@ def main_ours(args):
                      "unit": "GB/s", "frac": round(call_gbs / hbm, 4),
                      "traffic": tr["dram_bytes_per_launch"] if tr else None,
                      "peak_source": f"{peaks_src} hbm_gbs (copy)",
-                     "kernel": "pa_decode call (partition kernel + LSE merge)",
+                     "kernel": "pa_decode call (decode_kernel; split plans merge in the last CTA of each head group)",
                      "algorithmic_bytes_per_launch": r["per_layer_bytes"],
                      "avg_launch_ms": round(r["call_avg_ms"], 5)},
         "e2e": {"value": round(whole_job_gbs(world, r["step_bytes"], e2e_ms_step), 1),

@@ -86,8 +86,8 @@ const char *pa_strerror(int status);
  * recurrence of 19.6.2 (running max m, running sum l, unnormalised O); one
  * K/V page read serves all G query heads of its group.  Long contexts are
  * cut into partitions of `partition_tokens` tokens whose partial states
- * (m_p, l_p, O_p) are merged exactly (the exponent law of 19.6.2) by a second
- * kernel.  T = 0 writes zeros.
+ * (m_p, l_p, O_p) are merged exactly (the exponent law of 19.6.2) by the
+ * last CTA of the sequence's head group to finish.  T = 0 writes zeros.
  *
  *   q            device, [batch][n_q_heads][head_dim], dtype
  *   k_cache      device, [num_pages][n_kv_heads][page_size][head_dim], dtype
@@ -103,8 +103,10 @@ const char *pa_strerror(int status);
  *                many tokens and merged
  *   workspace    device, >= pa_decode_workspace_size(...) bytes, 16-byte
  *                aligned; may be NULL when that size is 0.  Holds the
- *                partial states; contents on entry do not matter.  Two calls
- *                that overlap on the GPU must not share a workspace.
+ *                partial states and arrival counters; contents on entry do
+ *                not matter (the call clears its counters on the stream
+ *                first).  Two calls that overlap on the GPU must not share a
+ *                workspace.
  * q, k_cache, v_cache, out and workspace must be 16-byte aligned.
  */
 int pa_decode(const void *q, const void *k_cache, const void *v_cache,
@@ -152,16 +154,18 @@ int pa_decode_partition_tokens(int batch, int n_q_heads, int n_kv_heads,
                                int max_blocks_per_seq, int partition_tokens);
 
 /* Workspace bytes pa_decode needs for the same arguments (0 when it runs in a
- * single pass).  Layout: float [batch][n_q_heads][n_parts][head_dim + 4],
- * each row (O_p[0..head_dim-1], m_p, l_p, 2 unused) with m_p in natural-log
- * units. */
+ * single pass).  Layout: float [batch][n_q_heads][n_parts][head_dim + 4] of
+ * rows (O[0..head_dim-1], m, l, 2 unused) with m in natural-log units --
+ * partial states of one partition or of the consecutive partitions one CTA
+ * holds -- then, at the next 16-byte boundary, one int32 arrival counter per
+ * (sequence, head group). */
 size_t pa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
                                 int head_dim, int page_size,
                                 int max_blocks_per_seq, int partition_tokens);
 
 /*
  * pa_merge_partials -- the exact merge of partition states on its own (the
- * same arithmetic pa_decode runs in its last partition's CTA).
+ * same arithmetic pa_decode runs in the last CTA of each head group).
  *
  * For row (b, h) with n = ceil(ctx_lens[b] / partition_tokens) valid parts
  * p < n (parts at p >= n are not read):
@@ -387,7 +391,8 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  Every call shares the one array and leaves its contents behind;
- * nothing in it needs to start at zero.  Calls that overlap on the GPU (two
+ * nothing in it needs to start at zero (each call clears its own arrival
+ * counters on the stream first).  Calls that overlap on the GPU (two
  * streams, or two host threads, with split-K plans) race on the array: the
  * caller must order them.
  */

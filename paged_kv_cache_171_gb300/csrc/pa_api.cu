@@ -305,7 +305,7 @@ size_t pa_decode_workspace_size(int batch, int n_q_heads, int n_kv_heads,
                   partition_tokens, &pp, &np))
     return 0;
   if (np <= 1) return 0;
-  return decode_partials_bytes(batch, n_q_heads, np, head_dim);
+  return decode_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, np);
 }
 
 }  // extern "C"
@@ -339,7 +339,7 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                    partition_tokens, &pp, &np, &wp);
   if (rc) return rc;
   if (np > 1) {
-    const size_t need = decode_partials_bytes(batch, n_q_heads, np, head_dim);
+    const size_t need = decode_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, np);
     if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PA_ERR_ALIGN;
   }

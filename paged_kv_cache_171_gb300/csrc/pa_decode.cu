@@ -6,17 +6,21 @@
 // (running max m, running sum l, unnormalised O).
 //
 // Work decomposition.  One CTA handles one (sequence, kv head, head tile,
-// partition): the GT query heads of a head tile share every K/V page it reads
+// key range): the GT query heads of a head tile share every K/V page it reads
 // (GQA reuse, "吞吐与延迟的系统模型" section 5: the kernel must reuse the shared
-// KV for the low-byte bound to hold).  Its NW warps take the partition's
-// pages round robin.  Each warp feeds itself: it keeps S pages in flight in
-// its own ring of shared-memory stages, filled by 2-D TMA loads (128-byte
-// swizzle) that complete on one mbarrier per stage, and issues the load for
-// page i+S as soon as page i has been consumed.  No warp waits for another
-// until the partition's end, where the warps' (m, l, O) states are merged in
-// shared memory with the exponent law of 19.6.2.  A sequence cut into several
-// partitions leaves one partial state per partition; merge_kernel combines
-// them exactly (same law).
+// KV for the low-byte bound to hold).  Its NW warps take the range's pages
+// round robin (one partition per CTA), or each warp owns whole consecutive
+// partitions (short partitions).  Each warp feeds itself: it keeps S pages in
+// flight in its own ring of shared-memory stages, filled by 2-D TMA loads
+// (128-byte swizzle) that complete on one mbarrier per stage, and issues the
+// load for page i+S as soon as page i has been consumed.  No warp waits for
+// another until the range's end, where the warps' (m, l, O) states are merged
+// in shared memory with the exponent law of 19.6.2.  A sequence cut over
+// several CTAs leaves one partial state per CTA; the last CTA of its
+// (sequence, head tile) to finish (an arrival counter) merges them all with
+// the same law, so no second kernel waits for the whole grid.  (When one CTA
+// holds all of a sequence's partitions, its warps write each partition's
+// state and the CTA folds them itself.)
 //
 // Per-page math, chosen by the group tile:
 //  * GT = 1 (MHA): CUDA cores.  Score phase lane = (token, half of head_dim):
@@ -54,7 +58,8 @@ struct DecodeParams {
   const int32_t *block_table;
   const int32_t *ctx_lens;
   float *out;
-  float *ws;  // partial states [B][Hq][n_parts][D + 4]
+  float *ws;   // split: partial states [B][Hq][n_parts][D + 4]
+  int *ctr;    // split: arrivals per (sequence, head tile), zero at launch
   int *status;
   float qscale;  // scale * log2(e)
   int n_q_heads, n_kv_heads, group, batch, max_blocks, num_pages;
@@ -446,8 +451,43 @@ __device__ __forceinline__ bool pages_mma(Ring &ring, int i_begin, int i_end,
   return ok;
 }
 
+// One CTA holds every partition of its (sequence, head tile), and its warps
+// have written their partitions' states to the workspace: after a barrier the
+// CTA folds partitions 0 .. n_valid - 1 of its GT rows into the output (the
+// exponent law of 19.6.2).
+template <int D, int GT, int NW>
+__device__ __forceinline__ void merge_own_partitions(const DecodeParams &p, size_t row0,
+                                                     int n_valid, int tid) {
+  __syncthreads();
+  constexpr int Q4 = D / 4;
+  for (int e = tid; e < GT * Q4; e += NW * 32) {
+    const float *base = p.ws + (row0 + e / Q4) * p.n_parts * (D + 4);
+    float m = -INFINITY, l = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < n_valid; ++c) {
+      const float *sp = base + static_cast<size_t>(c) * (D + 4);
+      const float2 ml = *reinterpret_cast<const float2 *>(sp + D);
+      const float4 o4 = reinterpret_cast<const float4 *>(sp)[e % Q4];
+      if (ml.y > 0.f) {  // a partition whose keys all had weight 0 adds nothing
+        const float mp = ml.x * kLog2e, mn = fmaxf(m, mp);
+        const float a = ex2(m - mn), f = ex2(mp - mn);  // a = 0 at m = -inf
+        acc = make_float4(acc.x * a + o4.x * f, acc.y * a + o4.y * f, acc.z * a + o4.z * f,
+                          acc.w * a + o4.w * f);
+        l = l * a + ml.y * f;
+        m = mn;
+      }
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    reinterpret_cast<float4 *>(p.out + (row0 + e / Q4) * D)[e % Q4] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+}
+
 // ---------------------------------------------------------------------------
-template <int D, int GT, bool BF16, int NW, int S, bool MMA>
+// SPLIT: several CTAs per (sequence, head tile), merged by the last to finish
+// (a separate instantiation, so one CTA per (sequence, head tile) carries
+// none of that code).
+template <int D, int GT, bool BF16, int NW, int S, bool MMA, bool SPLIT>
 __global__ void __launch_bounds__(NW * 32)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap,
@@ -479,24 +519,22 @@ __global__ void __launch_bounds__(NW * 32)
   KeySet ks;
   ks.init(T, p.sink, p.window);
   const int n_pages = ks.n_v;  // virtual pages of the attended keys
-  int pg0 = 0, pg1 = n_pages;  // this CTA's pages
-  if (ppw > 0) {
-    pg0 = blockIdx.x * NW * ppw * p.part_pages;
-    pg1 = min(n_pages, pg0 + NW * ppw * p.part_pages);
-    if (pg0 >= pg1) return;  // the merge writes zeros for an empty sequence
-  } else {
-    if (p.part_pages > 0) {
-      pg0 = blockIdx.x * p.part_pages;
-      pg1 = min(n_pages, pg0 + p.part_pages);
-    }
-    if (pg0 >= pg1) {
-      // Nothing to read.  An empty sequence owes zeros (partition 0 writes
-      // them); the merge never reads a partition past a sequence's end.
-      if (blockIdx.x == 0)
-        for (int i = tid; i < GT * D; i += NW * 32)
-          p.out[(static_cast<size_t>(b) * p.n_q_heads + h0) * D + i] = 0.f;
-      return;
-    }
+  // Pages per CTA (0: all of them), this CTA's pages, and how many CTAs of
+  // this (sequence, head tile) have any: those, and only those, arrive at
+  // the merge.
+  const int cta_pages = ppw > 0 ? NW * ppw * p.part_pages : p.part_pages;
+  int pg0 = 0, pg1 = n_pages;
+  if (cta_pages > 0) {
+    pg0 = blockIdx.x * cta_pages;
+    pg1 = min(n_pages, pg0 + cta_pages);
+  }
+  const int n_active = cta_pages > 0 ? (n_pages + cta_pages - 1) / cta_pages : 1;
+  if (pg0 >= pg1) {
+    // Nothing to read.  An empty sequence owes zeros (CTA 0 writes them).
+    if (blockIdx.x == 0)
+      for (int i = tid; i < GT * D; i += NW * 32)
+        p.out[(static_cast<size_t>(b) * p.n_q_heads + h0) * D + i] = 0.f;
+    return;
   }
 
   if (tid == 0) {
@@ -567,8 +605,9 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     };
-    if (ppw > 0) {
-      // ---- each partition's state goes straight from registers to memory
+    if (!SPLIT && ppw > 0) {
+      // ---- one CTA holds every partition: each one's state goes from
+      // registers to the workspace, then the CTA folds them into the output
       for (int k = 0; k < ppw && k * p.part_pages < ring.n_i; ++k) {
         reset();
         const bool ok = pages_mma<D, GT, BF16, NW, S>(
@@ -585,21 +624,24 @@ __global__ void __launch_bounds__(NW * 32)
         }
         if (!ok) break;
       }
+      merge_own_partitions<D, GT, NW>(p, row0, (n_pages + p.part_pages - 1) / p.part_pages, tid);
       return;
-    }
-    reset();
-    pages_mma<D, GT, BF16, NW, S>(ring, 0, ring.n_i, &kmap, &vmap, sbase + L::kQOff,
-                                  p.qscale, T, lane, m_r, l_r, o);
-    __syncthreads();  // every warp is done with its stages
-    if (r < GT) {
-      if ((lane & 3) == 0) {
-        mer_m[warp * GT + r] = m_r;
-        mer_l[warp * GT + r] = l_r;
-      }
+    } else {
+      // ---- one range per warp (a warp that owns partitions walks them as one)
+      reset();
+      pages_mma<D, GT, BF16, NW, S>(ring, 0, ring.n_i, &kmap, &vmap, sbase + L::kQOff,
+                                    p.qscale, T, lane, m_r, l_r, o);
+      __syncthreads();  // every warp is done with its stages
+      if (r < GT) {
+        if ((lane & 3) == 0) {
+          mer_m[warp * GT + r] = m_r;
+          mer_l[warp * GT + r] = l_r;
+        }
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n)
-        *reinterpret_cast<float2 *>(mer_o + (warp * GT + r) * D + n * 8 + k0) =
-            make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
+        for (int n = 0; n < D / 8; ++n)
+          *reinterpret_cast<float2 *>(mer_o + (warp * GT + r) * D + n * 8 + k0) =
+              make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
+      }
     }
   } else {
     constexpr int DPL = D / 32;
@@ -616,7 +658,7 @@ __global__ void __launch_bounds__(NW * 32)
     };
     float *p_s = reinterpret_cast<float *>(smem + L::kPOff) + warp * GT * 16;
     const float *q_s = reinterpret_cast<const float *>(smem + L::kQOff);
-    if (ppw > 0) {
+    if (!SPLIT && ppw > 0) {  // as in the tensor-core path
       for (int k = 0; k < ppw && k * p.part_pages < ring.n_i; ++k) {
         reset();
         const bool ok = pages_cuda_core<D, GT, BF16, NW, S>(
@@ -633,30 +675,32 @@ __global__ void __launch_bounds__(NW * 32)
         }
         if (!ok) break;
       }
+      merge_own_partitions<D, GT, NW>(p, row0, (n_pages + p.part_pages - 1) / p.part_pages, tid);
       return;
-    }
-    reset();
-    pages_cuda_core<D, GT, BF16, NW, S>(ring, 0, ring.n_i, &kmap, &vmap, q_s, p_s, T, lane, m,
-                                        lsum, O2);
-    __syncthreads();  // every warp is done with its stages
-    if (lane == 0) {
+    } else {
+      reset();
+      pages_cuda_core<D, GT, BF16, NW, S>(ring, 0, ring.n_i, &kmap, &vmap, q_s, p_s, T, lane,
+                                          m, lsum, O2);
+      __syncthreads();  // every warp is done with its stages
+      if (lane == 0) {
 #pragma unroll
-      for (int h = 0; h < GT; ++h) {
-        mer_m[warp * GT + h] = m[h];
-        mer_l[warp * GT + h] = lsum[h];
+        for (int h = 0; h < GT; ++h) {
+          mer_m[warp * GT + h] = m[h];
+          mer_l[warp * GT + h] = lsum[h];
+        }
       }
+#pragma unroll
+      for (int h = 0; h < GT; ++h)
+#pragma unroll
+        for (int k = 0; k < DPL / 2; ++k)
+          *reinterpret_cast<float2 *>(mer_o + (warp * GT + h) * D + lane * DPL + 2 * k) =
+              O2[h][k];
     }
-#pragma unroll
-    for (int h = 0; h < GT; ++h)
-#pragma unroll
-      for (int k = 0; k < DPL / 2; ++k)
-        *reinterpret_cast<float2 *>(mer_o + (warp * GT + h) * D + lane * DPL + 2 * k) =
-            O2[h][k];
   }
-  __syncthreads();
 
-  // ---- merge the NW warp states: final output, or this partition's state
-  const int part = blockIdx.x;
+  // ---- merge the NW warp states: final output, or this CTA's partial state
+  // (slot blockIdx.x of the row: the partition, or the CTA's partitions)
+  __syncthreads();
   for (int e = tid; e < GT * D; e += NW * 32) {
     const int h = e / D, d = e % D;
     float M = -INFINITY;
@@ -672,10 +716,10 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
     const size_t row = row0 + h;
-    if (p.n_parts == 1) {
+    if constexpr (!SPLIT) {
       p.out[row * D + d] = lt > 0.f ? o / lt : 0.f;
     } else {
-      float *dst = p.ws + (row * p.n_parts + part) * (D + 4);
+      float *dst = p.ws + (row * p.n_parts + blockIdx.x) * (D + 4);
       dst[d] = o;
       if (d == 0) {
         dst[D] = M * kLn2;  // natural-log units
@@ -683,6 +727,87 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
   }
+
+  if constexpr (SPLIT) {
+    // ---- the last of the n_active CTAs of this (sequence, head tile) to
+    // finish merges all their states (the same exponent law).  One
+    // thread arrives with an acquire-release add once the CTA's partial
+    // stores are issued (release: they are visible before the arrival
+    // counts; acquire: the last arrival sees every other CTA's), the barrier
+    // extending it to the CTA.
+    __shared__ int s_last;
+    __syncthreads();
+    const int grp = blockIdx.z * gridDim.y + blockIdx.y;
+    if (tid == 0) s_last = atomic_add_acq_rel_gpu(p.ctr + grp, 1) == n_active - 1;
+    __syncthreads();
+    if (!s_last) return;
+    // Thread t folds (row, float4 of head_dim) pairs t, t + 128, ... over the
+    // CTAs' states, loading 8 of them before folding any, so n CTAs cost
+    // about n / 8 round trips to L2.
+    const int n_valid = n_active;
+    constexpr int Q4 = D / 4, kPairs = (GT * Q4 + NW * 32 - 1) / (NW * 32), kBatch = 8;
+    float mm[kPairs], ll[kPairs];
+    float4 acc[kPairs];
+#pragma unroll
+    for (int j = 0; j < kPairs; ++j) {
+      mm[j] = -INFINITY;
+      ll[j] = 0.f;
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int c0 = 0; c0 < n_valid; c0 += kBatch) {
+      float2 ml[kPairs][kBatch];
+      float4 o4[kPairs][kBatch];
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j) {
+        const int e = tid + j * NW * 32;
+        const float *base = p.ws + (row0 + e / Q4) * p.n_parts * (D + 4);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          ml[j][u] = make_float2(-INFINITY, 0.f);
+          if (e < GT * Q4 && c0 + u < n_valid) {
+            const float *sp = base + static_cast<size_t>(c0 + u) * (D + 4);
+            ml[j][u] = __ldcg(reinterpret_cast<const float2 *>(sp + D));
+            o4[j][u] = __ldcg(reinterpret_cast<const float4 *>(sp) + e % Q4);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j)
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (ml[j][u].y > 0.f) {  // a CTA whose keys all had weight 0 adds nothing
+            const float mp = ml[j][u].x * kLog2e;
+            const float mn = fmaxf(mm[j], mp);
+            const float a = ex2(mm[j] - mn), f = ex2(mp - mn);  // a = 0 at m = -inf
+            acc[j].x = acc[j].x * a + o4[j][u].x * f;
+            acc[j].y = acc[j].y * a + o4[j][u].y * f;
+            acc[j].z = acc[j].z * a + o4[j][u].z * f;
+            acc[j].w = acc[j].w * a + o4[j][u].w * f;
+            ll[j] = ll[j] * a + ml[j][u].y * f;
+            mm[j] = mn;
+          }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kPairs; ++j) {
+      const int e = tid + j * NW * 32;
+      if (e < GT * Q4) {
+        const float inv = ll[j] > 0.f ? 1.f / ll[j] : 0.f;
+        reinterpret_cast<float4 *>(p.out + (row0 + e / Q4) * D)[e % Q4] =
+            make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
+      }
+    }
+    if (tid == 0) p.ctr[grp] = 0;  // left as the next call's clear finds it
+  }
+}
+
+// Clears a split pa_decode's arrival counters after every earlier kernel in
+// the stream (one of them may still be counting on the same workspace).
+__global__ void clear_counters_kernel(int *ctr, int n) {
+  griddep_release();
+  griddep_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    ctr[i] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -700,7 +825,7 @@ template <int D>
 __global__ void __launch_bounds__(128)
     merge_kernel(const float *__restrict__ parts, const int32_t *__restrict__ ctx,
                  float *__restrict__ out, int *status, int n_q_heads, int n_parts,
-                 int part_tokens, int prefill, int sink, int window) {
+                 int part_tokens, int prefill) {
   constexpr int W = D + 4, Q = D / 4, SL = 128 / Q;
   __shared__ float2 sml[SL];
   __shared__ __align__(16) float sacc[SL][D];
@@ -714,11 +839,7 @@ __global__ void __launch_bounds__(128)
     T = 0;
   }
   if (prefill) T += i + 1;
-  // partitions cut the attended keys' virtual pages (all pages without a window)
-  long span = T;
-  if (window >= 0 && sink + window < T)
-    span = 16L * (((sink + 15) >> 4) + (window > 0 ? ((T + 15) >> 4) - ((T - window) >> 4) : 0));
-  int n_valid = static_cast<int>((span + part_tokens - 1) / part_tokens);
+  int n_valid = static_cast<int>((T + part_tokens - 1) / part_tokens);
   if (n_valid > n_parts) {
     if (tid == 0 && blockIdx.x == 0) record_error(status, PA_ERR_BAD_CTX);
     n_valid = n_parts;
@@ -782,15 +903,19 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   constexpr int NW = kDecodeWarps, S = stages_per_warp<D>();
   constexpr bool MMA = GT >= 2;
   using L = DecodeSmem<D, GT, NW, S, MMA>;
-  auto kern = decode_kernel<D, GT, BF16, NW, S, MMA>;
-  static uint64_t attr_set = 0;  // one bit per device ordinal
+  const int gx = a.warp_parts > 0 ? (a.n_parts + NW * a.warp_parts - 1) / (NW * a.warp_parts)
+                                  : a.n_parts;
+  const bool split = gx > 1;  // else one CTA per (sequence, head tile)
+  auto kern = split ? decode_kernel<D, GT, BF16, NW, S, MMA, true>
+                    : decode_kernel<D, GT, BF16, NW, S, MMA, false>;
+  static uint64_t attr_set[2] = {0, 0};  // one bit per device ordinal and variant
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return PA_ERR_CUDA;
-  if (!(attr_set >> dev & 1)) {
+  if (!(attr_set[split] >> dev & 1)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kAlloc) != cudaSuccess)
       return PA_ERR_CUDA;
-    attr_set |= uint64_t(1) << dev;
+    attr_set[split] |= uint64_t(1) << dev;
   }
   CUtensorMap kmap, vmap;
   const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.n_kv_heads * 16;
@@ -803,6 +928,7 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   p.out = a.out;
   p.ws = a.workspace;
   p.status = a.status;
+  p.ctr = nullptr;
   p.qscale = a.scale * kLog2e;
   p.n_q_heads = a.n_q_heads;
   p.n_kv_heads = a.n_kv_heads;
@@ -815,19 +941,17 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   p.warp_parts = a.warp_parts;
   p.sink = a.sink;
   p.window = a.window;
-  const int gx = a.warp_parts > 0 ? (a.n_parts + NW * a.warp_parts - 1) / (NW * a.warp_parts)
-                                  : a.n_parts;
   const dim3 grid(gx, a.n_kv_heads * (p.group / GT), a.batch);
-  if (launch_pdl(kern, grid, dim3(NW * 32), L::kAlloc, stream, kmap, vmap, p) != cudaSuccess)
-    return PA_ERR_CUDA;
-  if (a.n_parts > 1) {
-    const dim3 mgrid(a.n_q_heads, a.batch);
-    if (launch_pdl(merge_kernel<D>, mgrid, dim3(128), 0, stream,
-                   static_cast<const float *>(a.workspace), a.ctx_lens, a.out, a.status,
-                   a.n_q_heads, a.n_parts, a.part_pages * 16, 0, a.sink, a.window) !=
-        cudaSuccess)
+  if (split) {
+    p.ctr = reinterpret_cast<int *>(reinterpret_cast<char *>(a.workspace) +
+                                    decode_counters_offset(a.batch, a.n_q_heads, a.n_parts, D));
+    const int n_ctr = static_cast<int>(grid.y * grid.z);
+    if (launch_pdl(clear_counters_kernel, dim3((n_ctr + 255) / 256), dim3(256), 0, stream,
+                   p.ctr, n_ctr) != cudaSuccess)
       return PA_ERR_CUDA;
   }
+  if (launch_pdl(kern, grid, dim3(NW * 32), L::kAlloc, stream, kmap, vmap, p) != cudaSuccess)
+    return PA_ERR_CUDA;
   return PA_OK;
 }
 
@@ -857,12 +981,10 @@ int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,
   const dim3 grid(n_q_heads, batch);
   if (head_dim == 128)
     merge_kernel<128><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                                n_q_heads, n_parts, partition_tokens, 0, 0,
-                                                -1);
+                                                n_q_heads, n_parts, partition_tokens, 0);
   else
     merge_kernel<64><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                               n_q_heads, n_parts, partition_tokens, 0, 0,
-                                               -1);
+                                               n_q_heads, n_parts, partition_tokens, 0);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -872,12 +994,10 @@ int launch_merge_rows(const float *partials, const int32_t *ctx_lens, float *out
   const dim3 grid(n_q_heads * n_new, batch);
   if (head_dim == 128)
     merge_kernel<128><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                                n_q_heads, n_parts, partition_tokens, 1, 0,
-                                                -1);
+                                                n_q_heads, n_parts, partition_tokens, 1);
   else
     merge_kernel<64><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                               n_q_heads, n_parts, partition_tokens, 1, 0,
-                                               -1);
+                                               n_q_heads, n_parts, partition_tokens, 1);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

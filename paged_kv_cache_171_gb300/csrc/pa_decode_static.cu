@@ -61,7 +61,8 @@ extern "C" int pa_decode_static_workspace(
     if (!scratch) return PA_ERR_CUDA;
   }
   // Every partial state the merge reads is written by the same call first,
-  // so the array never needs clearing.
+  // and pa_decode clears the arrival counters before its kernel runs, so the
+  // array never needs clearing by the caller.
   return pa_decode(q, k_cache, v_cache, block_table, ctx_lens, out, scale, n_q_heads,
                    n_kv_heads, head_dim, page_size, batch, max_blocks_per_seq,
                    num_pages, dtype, partition_tokens, scratch,

@@ -145,6 +145,16 @@ __device__ __forceinline__ void griddep_release() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ---- warp-level tensor-core fragments (ldmatrix + mma.sync m16n8k16)
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,

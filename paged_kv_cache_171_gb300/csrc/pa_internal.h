@@ -37,12 +37,28 @@ struct DecodeLaunch {
 
 constexpr int kDecodeWarps = 4;  // warps per decode CTA
 
+// Largest group tile (heads handled by one CTA) that divides the group size.
+inline int group_tile(int group) {
+  return (group % 8 == 0) ? 8 : (group % 4 == 0) ? 4 : (group % 2 == 0) ? 2 : 1;
+}
+
 int launch_decode(const DecodeLaunch &a, cudaStream_t stream);
 
 // Workspace of a split pa_decode: float partial states [B][Hq][n_parts][D + 4]
-// (O_p, m_p, l_p, two unused floats: rows stay 16-byte aligned).
+// (O_p, m_p, l_p, two unused floats: rows stay 16-byte aligned), then one int
+// arrival counter per (sequence, head tile) at the next 16-byte boundary (the
+// last CTA of a (sequence, head tile) to arrive merges its partitions).
 inline size_t decode_partials_bytes(int batch, int n_q_heads, int n_parts, int head_dim) {
   return static_cast<size_t>(batch) * n_q_heads * n_parts * (head_dim + 4) * sizeof(float);
+}
+inline size_t decode_counters_offset(int batch, int n_q_heads, int n_parts, int head_dim) {
+  return (decode_partials_bytes(batch, n_q_heads, n_parts, head_dim) + 15) & ~size_t(15);
+}
+inline size_t decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                     int n_parts) {
+  const int group = n_q_heads / n_kv_heads;
+  const size_t groups = static_cast<size_t>(batch) * n_kv_heads * (group / group_tile(group));
+  return decode_counters_offset(batch, n_q_heads, n_parts, head_dim) + groups * sizeof(int);
 }
 
 int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,
@@ -95,10 +111,6 @@ int *device_status(int device);
 int make_rows_map(CUtensorMap *map, const void *base, uint64_t rows,
                   int head_dim, int box_rows);
 
-// Largest group tile (heads handled by one CTA) that divides the group size.
-inline int group_tile(int group) {
-  return (group % 8 == 0) ? 8 : (group % 4 == 0) ? 4 : (group % 2 == 0) ? 2 : 1;
-}
 
 // Launch with programmatic stream serialisation (the kernel must call
 // griddep_wait() before it reads anything a predecessor may write).

@@ -82,9 +82,15 @@ def test_decode_rejects_bad_arguments(L, kw, code):
     assert _decode(L, **kw) == code
 
 
+def _group_tile(group):
+    return 8 if group % 8 == 0 else 4 if group % 4 == 0 else 2 if group % 2 == 0 else 1
+
+
 def _ws_bytes(b, hq, hkv, d, n_parts):
-    """batch * heads * parts * (D + 4) floats."""
-    return b * hq * n_parts * (d + 4) * 4
+    """batch * heads * parts * (D + 4) floats, then one int32 arrival counter
+    per (sequence, head group) at the next 16-byte boundary."""
+    part = b * hq * n_parts * (d + 4) * 4
+    return -(-part // 16) * 16 + b * hkv * ((hq // hkv) // _group_tile(hq // hkv)) * 4
 
 
 def test_workspace_size_matches_layout(L):

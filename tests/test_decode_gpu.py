@@ -87,6 +87,26 @@ def test_decode_long_random_lengths_all_partition_modes():
     assert pa.pa_last_device_error() == 0
 
 
+def test_decode_one_cta_holding_every_partition():
+    """Four 512-token partitions of 128-page tables: one CTA per (sequence,
+    head tile) whose four warps each own a partition and whose partial states
+    the CTA folds itself (no cross-CTA merge); ragged lengths leave some warps
+    without pages, and an empty sequence gives zeros."""
+    lens = [2048, 600, 1, 0, 1500, 1537]
+    for hq, hkv in [(32, 8), (16, 16)]:
+        kw = dict(layers=1, batch=len(lens), n_q_heads=hq, n_kv_heads=hkv, head_dim=128,
+                  page_size=16, ctx=lens, dtype="bf16", seed=41, max_blocks=128)
+        cpu = workloads.paged_case(**kw)
+        assert cpu.block_table.shape[2] == 128
+        assert pa.pa_decode_partition_tokens(len(lens), hq, hkv, 128, 16, 128, 512) == 512
+        ref = _oracle(cpu)
+        out = _run_decode(to_device(workloads.paged_case(**kw), "cuda"),
+                          partition_tokens=512).cpu().numpy()
+        assert_close(out, ref, f"{hq}/{hkv} one CTA, four partitions")
+        assert np.all(out[3] == 0.0)
+    assert pa.pa_last_device_error() == 0
+
+
 def test_merge_partials_matches_oracle_merge():
     """pa_merge_partials on its own, fed the oracle's per-chunk states."""
     lens = [1000, 1, 512, 0, 333]

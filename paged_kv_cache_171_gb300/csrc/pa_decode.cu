@@ -992,13 +992,13 @@ int launch_merge_rows(const float *partials, const int32_t *ctx_lens, float *out
                       int batch, int n_q_heads, int head_dim, int n_parts,
                       int partition_tokens, int n_new, cudaStream_t stream) {
   const dim3 grid(n_q_heads * n_new, batch);
-  if (head_dim == 128)
-    merge_kernel<128><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                                n_q_heads, n_parts, partition_tokens, 1);
-  else
-    merge_kernel<64><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
-                                               n_q_heads, n_parts, partition_tokens, 1);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const cudaError_t e =
+      head_dim == 128
+          ? launch_pdl(merge_kernel<128>, grid, dim3(128), 0, stream, partials, ctx_lens, out,
+                       status, n_q_heads, n_parts, partition_tokens, 1)
+          : launch_pdl(merge_kernel<64>, grid, dim3(128), 0, stream, partials, ctx_lens, out,
+                       status, n_q_heads, n_parts, partition_tokens, 1);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa

@@ -640,6 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_release();
+  griddep_wait();  // inputs may come from the previous kernel in the stream
 
   TcWork w;
   const int n_sub = p.group / GT;
@@ -798,8 +800,8 @@ int launch_tc_t(const PrefillLaunch &a, cudaStream_t stream) {
   constexpr int BQ = kRows / GT;
   const dim3 grid(((a.n_new + 2 * BQ - 1) / (2 * BQ)) * p.n_parts,
                   a.n_kv_heads * (p.group / GT), a.batch);
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(kmap, vmap, p);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_pdl(kern, grid, dim3(kThreads), L::kAlloc, stream, kmap, vmap, p) != cudaSuccess)
+    return PA_ERR_CUDA;
   if (p.n_parts > 1)
     return launch_merge_rows(a.workspace, a.ctx_lens, a.out, a.status, a.batch, a.n_q_heads,
                              D, p.n_parts, a.part_tokens, a.n_new, stream);

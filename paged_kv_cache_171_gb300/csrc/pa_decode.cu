@@ -945,9 +945,7 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   if (split) {
     p.ctr = reinterpret_cast<int *>(reinterpret_cast<char *>(a.workspace) +
                                     decode_counters_offset(a.batch, a.n_q_heads, a.n_parts, D));
-    const int n_ctr = static_cast<int>(grid.y * grid.z);
-    if (launch_pdl(clear_counters_kernel, dim3((n_ctr + 255) / 256), dim3(256), 0, stream,
-                   p.ctr, n_ctr) != cudaSuccess)
+    if (launch_clear_counters(p.ctr, static_cast<int>(grid.y * grid.z), stream) != PA_OK)
       return PA_ERR_CUDA;
   }
   if (launch_pdl(kern, grid, dim3(NW * 32), L::kAlloc, stream, kmap, vmap, p) != cudaSuccess)
@@ -973,6 +971,13 @@ int launch_decode(const DecodeLaunch &a, cudaStream_t stream) {
                   : launch_decode_d<128, false>(a, stream);
   return a.bf16 ? launch_decode_d<64, true>(a, stream)
                 : launch_decode_d<64, false>(a, stream);
+}
+
+int launch_clear_counters(int *ctr, int n, cudaStream_t stream) {
+  return launch_pdl(clear_counters_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, ctr,
+                    n) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,

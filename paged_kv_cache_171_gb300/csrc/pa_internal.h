@@ -95,6 +95,10 @@ inline size_t prefill_partials_bytes(int batch, int n_new, int n_q_heads, int n_
          sizeof(float);
 }
 
+// Clears n arrival counters of a split pa_decode after every earlier kernel in
+// the stream (one CTA per 256 counters, programmatic dependent launch).
+int launch_clear_counters(int *ctr, int n, cudaStream_t stream);
+
 // Merge of prefill rows: row (b, i, h) of q_len = n_new queries saw
 // ctx_lens[b] + i + 1 keys.
 int launch_merge_rows(const float *partials, const int32_t *ctx_lens, float *out, int *status,

@@ -256,8 +256,8 @@ int pa_prefill_paged_split(const void *q, const void *k_cache, const void *v_cac
  * The key-range size pa_prefill_paged_split uses for these shapes (0 = no
  * split), or a negative PA_ERR_* for invalid arguments.  The automatic
  * choice splits only when there are fewer row-tile CTAs than SMs, into
- * ranges of at least 512 keys, as many as keep the grid within two waves of
- * one CTA per SM.
+ * ranges of at least 512 keys: as many as fit one wave of one CTA per SM,
+ * or, when that wave would leave more than 30% of the SMs idle, as fill two.
  */
 int pa_prefill_partition_tokens(int batch, int n_new, int n_q_heads, int n_kv_heads,
                                 int head_dim, int page_size, int max_blocks_per_seq,

@@ -215,9 +215,11 @@ int decode_plan(int batch, int n_q_heads, int n_kv_heads, int max_blocks,
 // Key-range partitions of the chunked prefill (multiples of 128 keys, the
 // kernel's key tile).  A CTA holds two row tiles of 128 (query, head) rows
 // and one CTA fits an SM; with fewer CTAs than SMs, a sequence's keys are cut
-// into as many ranges as keep the grid within two full waves (equal ranges
-// finish together, so a third, nearly empty wave would cost a whole range),
-// each range at least 512 keys.
+// into as many ranges as fit one wave of CTAs (equal ranges finish together,
+// and every further wave pays the CTAs' start-up and a bigger merge again:
+// at 4 x 32k keys, 64/8 heads, 128 CTAs in one wave ran 96 us, 288 in two
+// waves 106 us), or as fill two waves when one wave would leave more than
+// 30% of the SMs idle; each range at least 512 keys.
 int prefill_plan(int batch, int n_new, int n_q_heads, int n_kv_heads, int max_blocks,
                  int partition_tokens, int *part_tokens, int *n_parts) {
   constexpr int kTile = 128;
@@ -232,7 +234,8 @@ int prefill_plan(int batch, int n_new, int n_q_heads, int n_kv_heads, int max_bl
                           ((n_new + rows_per_cta - 1) / rows_per_cta);
     const int sms = sm_count() > 0 ? sm_count() : 148;
     if (items < sms) {
-      const int64_t want = (2 * sms) / items;
+      const int64_t one_wave = sms / items;
+      const int64_t want = 10 * items * one_wave >= 7 * sms ? one_wave : (2 * sms) / items;
       per = (max_tokens + want - 1) / want;
       per = (per + kTile - 1) / kTile * kTile;
       if (per < 4 * kTile) per = 4 * kTile;

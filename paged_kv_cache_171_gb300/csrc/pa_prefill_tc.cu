@@ -442,7 +442,8 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
   const int nt = w.n_tiles[x];
 
   bool bad = false;
-  float m = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float m = -INFINITY;
+  float2 lp = make_float2(0.f, 0.f);  // running sums of the even and odd keys
   for (int j = 0; j < nt; ++j) {
     // ping-pong: wait for the other tile's turn before this one (where the
     // other tile has that many key tiles)
@@ -488,10 +489,10 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
       const float mn = fmaxf(m, cand);
       corr = ex2(m - mn);  // 0 while m was still -inf
       m = mn;
-      l0 *= corr;
-      l1 *= corr;
+      lp = __fmul2_rn(lp, make_float2(corr, corr));
     }
     const float nm = m == -INFINITY ? 0.f : -m;  // nothing seen yet: weights are 0
+    const float2 qs2 = make_float2(qs, qs), nm2 = make_float2(nm, nm);
 
     // ---- P = 2^(s qs - m) as head + remainder, over the S columns; each
     // half of the keys is handed to the MMA warp as soon as it is written
@@ -500,13 +501,15 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
       uint32_t phi[16], plo[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const float p0 = ex2(fmaf(__uint_as_float(s[32 * ch + 2 * k]), qs, nm));
-        const float p1 = ex2(fmaf(__uint_as_float(s[32 * ch + 2 * k + 1]), qs, nm));
-        l0 += p0;
-        l1 += p1;
-        phi[k] = pack2<BF16>(p0, p1);
-        const float2 hr = unpack2<BF16>(phi[k]);
-        plo[k] = pack2<BF16>(p0 - hr.x, p1 - hr.y);
+        // packed fp32x2 arithmetic: one instruction per key pair
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[32 * ch + 2 * k]),
+                                                __uint_as_float(s[32 * ch + 2 * k + 1])),
+                                    qs2, nm2);
+        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+        lp = __fadd2_rn(lp, pp);
+        phi[k] = pack2<BF16>(pp.x, pp.y);
+        const float2 d = __ffma2_rn(unpack2<BF16>(phi[k]), make_float2(-1.f, -1.f), pp);
+        plo[k] = pack2<BF16>(d.x, d.y);  // the remainder p - head, exact before rounding
       }
       if (!SR) {
         tc::st16(tSx + 16 * ch, phi);
@@ -539,7 +542,7 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
   if (nt == 0) return;
   if (!bad) bad = !warp_wait(bar(kBarO + x), 0, abort_flag);
   if (bad && lane == 0) raise_abort(p.status, abort_flag);
-  float l = l0 + l1, ca = 1.f, cb = 0.f;
+  float l = lp.x + lp.y, ca = 1.f, cb = 0.f;
   if (IL) {
     // both warpgroups always meet here, failed or not, and all of them take
     // the same decision

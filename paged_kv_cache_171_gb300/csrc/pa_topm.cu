@@ -93,6 +93,33 @@ __device__ __forceinline__ void load_run(const float *__restrict__ scores, int n
   }
 }
 
+// Inclusive prefix sum of v over the CTA's NT threads (NT a multiple of 32,
+// at most 1024; once per kernel): a shuffle scan inside each warp, then one
+// over the warp totals -- two barriers.
+template <int NT>
+__device__ __forceinline__ uint32_t block_scan_incl(uint32_t v) {
+  __shared__ uint32_t wsum[NT / 32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  if (lane == 31) wsum[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t w = lane < NT / 32 ? wsum[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += u;
+    }
+    if (lane < NT / 32) wsum[lane] = w;
+  }
+  __syncthreads();
+  return v + (wid > 0 ? wsum[wid - 1] : 0u);
+}
+
 // First digit: histogram of the top 11 key bits over every candidate
 // element.  Each quarter of the CTA's warps counts into its own copy in
 // shared memory (fewer collisions on the few crowded bins), summed at the end.
@@ -154,7 +181,6 @@ __global__ void __launch_bounds__(1024)
   griddep_wait();  // the previous launch of the stream has completed
   griddep_release();
   constexpr int kPer = BINS / 1024;
-  __shared__ uint32_t c[1024];
   const int t = threadIdx.x;
   uint32_t v[kPer], sum = 0;
 #pragma unroll
@@ -162,17 +188,10 @@ __global__ void __launch_bounds__(1024)
     v[i] = hist[kPer * t + i];
     sum += v[i];
   }
-  c[t] = sum;
-  __syncthreads();
-  for (int o = 1; o < 1024; o <<= 1) {  // inclusive scan (Hillis-Steele)
-    const uint32_t u = t >= o ? c[t - o] : 0u;
-    __syncthreads();
-    c[t] += u;
-    __syncthreads();
-  }
+  const uint32_t incl = block_scan_incl<1024>(sum);
   const uint32_t k = st->k_rem;
-  uint32_t before = c[t] - sum;
-  if (before < k && k <= c[t]) {  // exactly one thread
+  uint32_t before = incl - sum;
+  if (before < k && k <= incl) {  // exactly one thread
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       if (before < k && k <= before + v[i]) {
@@ -400,30 +419,38 @@ __global__ void __launch_bounds__(1024)
                      TopmState *__restrict__ st) {
   griddep_wait();  // the previous launch of the stream has completed
   griddep_release();
-  __shared__ uint32_t c[1024];
-  const int per = (n_chunks + 1023) / 1024;
+  // runs of a multiple of 4 counts, loaded 16 bytes at a time (the counts
+  // start 16-byte aligned)
+  const int per = ((n_chunks + 1023) / 1024 + 3) & ~3;
   const int lo = threadIdx.x * per, hi = min(n_chunks, lo + per);
+  auto quad = [&](int i) {
+    if (i + 4 <= hi) return *reinterpret_cast<const uint4 *>(tiecnt + i);
+    return make_uint4(i < hi ? tiecnt[i] : 0u, i + 1 < hi ? tiecnt[i + 1] : 0u,
+                      i + 2 < hi ? tiecnt[i + 2] : 0u, 0u);
+  };
   uint32_t sum = 0;
-  for (int i = lo; i < hi; ++i) sum += tiecnt[i];
-  c[threadIdx.x] = sum;
-  __syncthreads();
-  for (int o = 1; o < 1024; o <<= 1) {
-    const uint32_t u = threadIdx.x >= o ? c[threadIdx.x - o] : 0u;
-    __syncthreads();
-    c[threadIdx.x] += u;
-    __syncthreads();
+#pragma unroll 4
+  for (int i = lo; i < hi; i += 4) {
+    const uint4 v = quad(i);
+    sum += v.x + v.y + v.z + v.w;
   }
   const uint32_t r = st->k_rem;
-  uint32_t run = c[threadIdx.x] - sum;
+  uint32_t run = block_scan_incl<1024>(sum) - sum;
   if (run < r && r <= run + sum) {  // exactly one thread
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t v = tiecnt[i];
-      if (run < r && r <= run + v) {
-        st->tie_chunk = static_cast<uint32_t>(i);
-        st->tie_rank = r - run;
-        break;
+    for (int i = lo; i < hi; i += 4) {
+      const uint4 q = quad(i);
+      const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+      bool found = false;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (!found && run < r && r <= run + v[u]) {
+          st->tie_chunk = static_cast<uint32_t>(i + u);
+          st->tie_rank = r - run;
+          found = true;
+        }
+        if (!found) run += v[u];
       }
-      run += v;
+      if (found) break;
     }
   }
 }
@@ -447,16 +474,7 @@ __global__ void __launch_bounds__(kThreads)
     if (++t == N) t = 0;
   }
   const uint32_t ties = __popc(tie_bits);
-  __shared__ uint32_t c[kThreads];
-  c[threadIdx.x] = ties;
-  __syncthreads();
-  for (int o = 1; o < kThreads; o <<= 1) {
-    const uint32_t u = threadIdx.x >= o ? c[threadIdx.x - o] : 0u;
-    __syncthreads();
-    c[threadIdx.x] += u;
-    __syncthreads();
-  }
-  const uint32_t before = c[threadIdx.x] - ties;
+  const uint32_t before = block_scan_incl<kThreads>(ties) - ties;
   if (before < want && want <= before + ties) {  // exactly one thread
     uint32_t bits = tie_bits;
     for (uint32_t k = before + 1; k < want; ++k) bits &= bits - 1;  // drop earlier ties

@@ -499,17 +499,28 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
 #pragma unroll
     for (int ch = 0; ch < kKeys / 32; ++ch) {  // keys 32 ch .. 32 ch + 31
       uint32_t phi[16], plo[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        // packed fp32x2 arithmetic: one instruction per key pair
+      // packed fp32x2 arithmetic: one instruction per key pair; split rows:
+      // the warps of rows 0-63 store only the head term, so only the
+      // remainder warps (rows 64-127) compute the remainder
+      auto head = [&](int k) {
         const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[32 * ch + 2 * k]),
                                                 __uint_as_float(s[32 * ch + 2 * k + 1])),
                                     qs2, nm2);
         const float2 pp = make_float2(ex2(x.x), ex2(x.y));
         lp = __fadd2_rn(lp, pp);
         phi[k] = pack2<BF16>(pp.x, pp.y);
-        const float2 d = __ffma2_rn(unpack2<BF16>(phi[k]), make_float2(-1.f, -1.f), pp);
-        plo[k] = pack2<BF16>(d.x, d.y);  // the remainder p - head, exact before rounding
+        return pp;
+      };
+      if (!SR || rem) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 pp = head(k);
+          const float2 d = __ffma2_rn(unpack2<BF16>(phi[k]), make_float2(-1.f, -1.f), pp);
+          plo[k] = pack2<BF16>(d.x, d.y);  // the remainder p - head, exact before rounding
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) head(k);
       }
       if (!SR) {
         tc::st16(tSx + 16 * ch, phi);

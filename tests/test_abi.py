@@ -166,6 +166,18 @@ def test_prefill_split_plan_and_workspace(L):
     assert L.pa_prefill_workspace_size(4, 512, 32, 8, 128, 16, 545, 0) == 0
 
 
+def test_prefill_auto_plan_is_one_full_wave(L):
+    """The automatic key-range plan: with 32 row-tile CTAs (4 sequences x 8 kv
+    heads, a verify-sized chunk of 4 tokens over 32k keys) four ranges of 8320
+    keys give 128 CTAs, one wave on a GPU of 148-152 SMs; a chunk whose row
+    tiles already fill most SMs is not split."""
+    pt = L.pa_prefill_partition_tokens(4, 4, 64, 8, 128, 16, 2049, 0)
+    assert pt == 8320 and -(-2049 * 16 // pt) == 4
+    assert L.pa_prefill_partition_tokens(4, 8, 64, 8, 128, 16, 2049, 0) == 8320
+    # 120 row-tile CTAs (15 sequences x 8 kv heads): one wave as they are
+    assert L.pa_prefill_partition_tokens(15, 4, 64, 8, 128, 16, 2049, 0) == 0
+
+
 def test_prefill_split_rejects_bad_arguments(L):
     P = FAKE
     f = ctypes.c_float(0.1)

@@ -107,6 +107,36 @@ def test_decode_one_cta_holding_every_partition():
     assert pa.pa_last_device_error() == 0
 
 
+def test_split_decode_ignores_workspace_contents_and_streams_do_not_interfere():
+    """The split plan's arrival counters live in the workspace: a workspace
+    full of garbage (every counter -1) gives the right result, and two calls
+    on two streams with their own workspaces run concurrently without
+    affecting each other."""
+    lens = [4096, 2500, 17, 1000]
+    kw = dict(layers=1, batch=len(lens), n_q_heads=32, n_kv_heads=8, head_dim=128,
+              page_size=16, ctx=lens, dtype="bf16", seed=43)
+    ref = _oracle(workloads.paged_case(**kw))
+    dev = to_device(workloads.paged_case(**kw), "cuda")
+    B, hq, hkv, D, mb = len(lens), 32, 8, 128, dev.block_table.shape[2]
+    for pt in (512, 256):
+        ws_bytes = pa.pa_decode_workspace_size(B, hq, hkv, D, 16, mb, pt)
+        assert ws_bytes > 0
+        wss = [torch.full((ws_bytes,), 0xFF, dtype=torch.uint8, device="cuda") for _ in range(2)]
+        outs = [torch.empty((B, hq, D), dtype=torch.float32, device="cuda") for _ in range(2)]
+        streams = [torch.cuda.Stream() for _ in range(2)]
+        torch.cuda.synchronize()
+        for _ in range(3):
+            for ws, out, st in zip(wss, outs, streams):
+                with torch.cuda.stream(st):
+                    pa.decode(dev.q[0], dev.k_cache, dev.v_cache, dev.block_table[0],
+                              dev.ctx_lens, dev.scale, partition_tokens=pt, out=out,
+                              workspace=ws, stream=st.cuda_stream)
+        torch.cuda.synchronize()
+        for out in outs:
+            assert_close(out.cpu().numpy(), ref, f"part={pt}, garbage workspace, two streams")
+    assert pa.pa_last_device_error() == 0
+
+
 def test_merge_partials_matches_oracle_merge():
     """pa_merge_partials on its own, fed the oracle's per-chunk states."""
     lens = [1000, 1, 512, 0, 333]

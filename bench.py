@@ -1,12 +1,17 @@
 #!/usr/bin/env python3
 """Benchmark of the paged GQA decode step on GB300.
 
-Headline workload (one "step" = one decode step of a 32-layer model): for each
-of 32 layers, pa_append_kv writes the step's new K/V row of every sequence
-into its page, then pa_decode attends each query head over the 4096 cached
-tokens (paged gather, online softmax, split-K partitions and their exact
-merge).  LLaMA-7B-shaped: batch 8, 32 query = 32 KV heads, head_dim 128, fp16
-KV, page_size 16, one shuffled pool of 65,536 pages.  Synthetic seeded data.
+Headline workload (one "step" = one decode step of a 32-layer model): the
+GQA continuous-batching batch, the largest decode workload that the pages
+describe.  For each of 32 layers, pa_append_kv writes the step's new K/V row
+of every sequence into its page, then pa_decode attends each query head over
+the sequence's cached tokens (paged gather, online softmax, split-K
+partitions and their exact merge).  64 sequences with seeded lengths drawn
+uniformly from [128, 8192], 32 query heads sharing 8 KV heads (GQA-4),
+head_dim 128, bf16 KV, page_size 16, random block tables, Q drawn N(0,1) x 2
+(peaky softmax).  The LLaMA-7B-shaped step (batch 8, 32/32 heads, context
+4096, fp16) is measured the same way as a second block of the line.
+Synthetic seeded data.
 
 Metric: decode-attention HBM GB/s (algorithmic bytes = unique KV bytes read +
 Q + fp32 output, per (sequence, layer)) and sequences*layers per second.
@@ -32,7 +37,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention HBM GB/s and % of GB300 HBM roofline; sequences·layers/sec"
-HEADLINE = "llama7b_b8_ctx4096"
+HEADLINE = "gqa4_b64_ragged"
+SECOND = "llama7b_b8_ctx4096"
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -83,17 +89,18 @@ def measured_peaks():
                 "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def traffic_record(kernel_file):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (sha256 of the .cu file), else None."""
+def traffic_record(workload, kernel_file="pa_decode.cu"):
+    """DRAM bytes per launch of `workload`'s dominant kernel from the
+    committed ncu summary, if it was taken on the current kernel source
+    (sha256 of the .cu file), else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     src = os.path.join(ROOT, "paged_kv_cache_171_gb300", "csrc", kernel_file)
     try:
         with open(path) as f:
             rec = json.load(f)
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        ent = rec.get(kernel_file)
-        if ent and ent.get("source_sha256") == sha:
+        ent = rec.get(workload)
+        if ent and ent.get("kernel_file") == kernel_file and ent.get("source_sha256") == sha:
             return ent
     except (OSError, ValueError):
         pass
@@ -174,15 +181,17 @@ def gpu_uuid(torch):
 # ---------------------------------------------------------------------------
 # our arm
 
-def run_headline(torch, pa, workloads, args, rank, world):
-    cfg = workloads.CONFIGS[HEADLINE]
+def run_decode_step(torch, pa, workloads, name, args, rank, world):
+    """The decode step of one 32-layer workload: per layer, pa_append_kv of
+    the step's token, then pa_decode over every cached token."""
+    cfg = workloads.CONFIGS[name]
     dev = torch.device("cuda", torch.cuda.current_device())
-    case = workloads.config_case(HEADLINE, device=dev)
+    case = workloads.config_case(name, device=dev)
     L, B = case.layers, case.q.shape[1]
     hq, hkv, D = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
     pages = case.k_cache.shape[0]
     mb = case.block_table.shape[2]
-    ctx = case.ctx_lens                      # every sequence holds 4096 tokens
+    ctx = case.ctx_lens                      # tokens held, the step's included
     pos = (ctx - 1).to(torch.int32)          # the step's token is the last one
     seq_idx = torch.arange(B, dtype=torch.int32, device=dev)
     k_new, v_new = workloads.new_tokens(L * B, hkv, D, cfg["dtype"], seed=cfg["seed"] + 1,
@@ -310,6 +319,7 @@ def run_headline(torch, pa, workloads, args, rank, world):
     assert pa.pa_last_device_error() == 0
 
     res = dict(
+        name=name, cfg=cfg,
         case=case, ms=ms_max, step_bytes=step_bytes, per_layer_bytes=per_layer_bytes,
         call_avg_ms=call_avg_ms, clocks=clocks, part=part, L=L, B=B,
         launches=args.steps * L * launches_per_layer,
@@ -659,10 +669,11 @@ def run_topm(torch, pa, steps, warmup, peaks, L=32, H=32, N=32768):
 
 
 def cpu_baseline_sample(torch, case, cfg, layers_budget_s=10.0):
-    """The float64 oracle, as it stands, on whole layers of the headline
-    workload until ~budget seconds pass (at least one layer)."""
+    """The float64 oracle, as it stands, on whole layers of a decode
+    workload (every sequence and head of the layer) until ~budget seconds
+    pass (at least one layer)."""
     import oracle
-    from tests.gpu_support import compact_host_copy  # re-indexing only
+    from workloads import compact_host_copy  # re-indexing only
     B = case.q.shape[1]
     hq, hkv, D = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
     threads = oracle.max_threads()
@@ -679,8 +690,64 @@ def cpu_baseline_sample(torch, case, cfg, layers_budget_s=10.0):
     return {"value": round(bytes_done / t_total / 1e9, 3), "unit": "GB/s",
             "cores": threads, "kind": "oracle",
             "sample": f"{done_layers} of {case.layers} layers x {B} sequences "
-                      f"(all heads, full 4096-token contexts), float64, OpenMP",
+                      f"(all heads, every cached token), float64, OpenMP",
             "seconds": round(t_total, 2)}
+
+
+def describe(name, cfg):
+    """One line naming a decode workload by what it is."""
+    ctx = cfg["ctx"]
+    ctx_s = (f"context ~ U[{ctx[0]}, {ctx[1]}] seeded" if isinstance(ctx, tuple)
+             else f"context {ctx}")
+    pool = (f"shuffled pool of {cfg['pool_pages']} pages" if cfg.get("pool_pages")
+            else "random block tables")
+    qm = f", Q x {cfg['q_mul']:g}" if cfg.get("q_mul", 1.0) != 1.0 else ""
+    return (f"{name}: decode step of {cfg['layers']} layers x (pa_append_kv + pa_decode), "
+            f"batch {cfg['batch']}, {cfg['n_q_heads']} q heads / {cfg['n_kv_heads']} kv "
+            f"heads, head_dim {cfg['head_dim']}, {ctx_s}, {cfg['dtype']} KV, page_size "
+            f"{cfg['page_size']}, {pool}{qm}")
+
+
+def step_block(r, args, world, peaks, peaks_src):
+    """value, roofline and e2e of one measured decode step (run_decode_step)."""
+    ms_step = r["ms"] / args.steps
+    value = whole_job_gbs(world, r["step_bytes"], ms_step)
+    seq_layers = world * r["L"] * r["B"] / (ms_step * 1e-3)
+    call_gbs = r["per_layer_bytes"] / (r["call_avg_ms"] * 1e-3) / 1e9
+    e2e_ms_step = r["e2e_ms"] / args.steps
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    tr = traffic_record(r["name"])
+    cfg = r["cfg"]
+    return {
+        "value": round(value, 1), "unit": "GB/s", "ms_per_step": round(ms_step, 4),
+        "dtype": "f32",
+        "data": f"synthetic (seeded N(0,1), rounded to {cfg['dtype']})",
+        "config": {
+            "workload": describe(r["name"], cfg),
+            "kv_dtype": cfg["dtype"], "accumulate": "f32", "out_dtype": "f32",
+            "partition_tokens": r["part"],
+            "l2": f"inputs larger than L2 ({r['step_bytes'] / 1e9:.1f} GB of KV per step "
+                  "vs 129 MB); no flush",
+            "bytes_per_step": r["step_bytes"],
+            "context_tokens_per_layer": sum(r["ctx_list"]),
+        },
+        "seq_layers_per_s": round(seq_layers, 1),
+        "frac_of_hbm_peak": round(value / world / hbm, 4),
+        "roofline": {"bound": "hbm", "achieved": round(call_gbs, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(call_gbs / hbm, 4),
+                     "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                     "peak_source": f"{peaks_src} hbm_gbs (copy)",
+                     "kernel": "pa_decode call (decode_kernel; split plans merge in the "
+                               "last CTA of each head group)",
+                     "algorithmic_bytes_per_launch": r["per_layer_bytes"],
+                     "avg_launch_ms": round(r["call_avg_ms"], 5),
+                     "traffic_capture": tr["capture"] if tr else None},
+        "e2e": {"value": round(whole_job_gbs(world, r["step_bytes"], e2e_ms_step), 1),
+                "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms_step, 4)},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
 
 
 # ---------------------------------------------------------------------------
@@ -727,53 +794,29 @@ def main_ours(args):
     pa_build.build()
     rank, world = init_dist(torch, args)
     peaks, peaks_src = measured_peaks()
-    r = run_headline(torch, pa, workloads, args, rank, world)
-    case = r["case"]
-    ms_step = r["ms"] / args.steps
-    value = whole_job_gbs(world, r["step_bytes"], ms_step)
-    seq_layers = world * r["L"] * r["B"] / (ms_step * 1e-3)
-    call_gbs = r["per_layer_bytes"] / (r["call_avg_ms"] * 1e-3) / 1e9
-    e2e_ms_step = r["e2e_ms"] / args.steps
     hbm = peaks.get("hbm_gbs", 6800.0)
-    tr = traffic_record("pa_decode.cu")
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded N(0,1), rounded to fp16)",
-        "config": {
-            "workload": f"{HEADLINE}: decode step of 32 layers x (pa_append_kv + "
-                        "pa_decode), batch 8, 32 q heads / 32 kv heads, head_dim 128, "
-                        "context 4096, fp16 KV, page_size 16, shuffled pool of 65536 "
-                        "pages",
-            "kv_dtype": "fp16", "accumulate": "f32", "out_dtype": "f32",
-            "partition_tokens": r["part"],
-            "l2": "inputs larger than L2 (17.2 GB of KV per step vs 129 MB); no flush",
-            "bytes_per_step": r["step_bytes"],
-        },
-        "seq_layers_per_s": round(seq_layers, 1),
-        "frac_of_hbm_peak": round(value / world / hbm, 4),
-        "roofline": {"bound": "hbm", "achieved": round(call_gbs, 1), "peak": hbm,
-                     "unit": "GB/s", "frac": round(call_gbs / hbm, 4),
-                     "traffic": tr["dram_bytes_per_launch"] if tr else None,
-                     "peak_source": f"{peaks_src} hbm_gbs (copy)",
-                     "kernel": "pa_decode call (decode_kernel; split plans merge in the last CTA of each head group)",
-                     "algorithmic_bytes_per_launch": r["per_layer_bytes"],
-                     "avg_launch_ms": round(r["call_avg_ms"], 5)},
-        "e2e": {"value": round(whole_job_gbs(world, r["step_bytes"], e2e_ms_step), 1),
-                "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
-                "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms_step, 4)},
-        "gpu_launches": r["launches"],
-        "clocks": r["clocks"],
-    }
+    r = run_decode_step(torch, pa, workloads, HEADLINE, args, rank, world)
+    blk = step_block(r, args, world, peaks, peaks_src)
+    line = {"metric": METRIC, "value": blk.pop("value"), "unit": blk.pop("unit"),
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": blk.pop("ms_per_step"), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None}
+    line.update(blk)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_sample(torch, case, workloads.CONFIGS[HEADLINE])
-    del case, r
+        line["cpu_baseline"] = cpu_baseline_sample(torch, r["case"], r["cfg"])
+    del r
     torch.cuda.empty_cache()
     if not args.only_headline:
+        # the LLaMA-7B-shaped step, measured the same way (a block of its own)
+        r2 = run_decode_step(torch, pa, workloads, SECOND, args, rank, world)
+        blk2 = step_block(r2, args, world, peaks, peaks_src)
+        blk2["steps"], blk2["warmup"] = args.steps, args.warmup
+        if rank == 0 and not args.no_cpu_baseline:
+            blk2["cpu_baseline"] = cpu_baseline_sample(torch, r2["case"], r2["cfg"])
+        line["second_workload"] = blk2
+        del r2
+        torch.cuda.empty_cache()
         other = {}
-        other["gqa4_b64_ragged"] = run_other_decode(torch, pa, workloads,
-                                                    "gqa4_b64_ragged", 5, 3)
         other["gqa8_b4_ctx32k"] = run_other_decode(torch, pa, workloads,
                                                    "gqa8_b4_ctx32k", 20, 5, 512)
         other["mha_b1_ctx512"] = run_other_decode(torch, pa, workloads,
@@ -794,7 +837,8 @@ def main_ours(args):
 
 
 def main_reference(args):
-    """The float64 oracle as the reference arm, on the host cores."""
+    """The float64 oracle as the reference arm, on the host cores: the
+    headline workload, one whole layer (every sequence and head) per step."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -802,11 +846,9 @@ def main_reference(args):
         return
     import oracle
     import workloads
-    oracle.build.build() if hasattr(oracle, "build") else None
     cfg = workloads.CONFIGS[HEADLINE]
-    # the same workload, built on the host; each step = one whole layer
-    # (8 sequences x 32 heads x 4096 tokens) through the oracle
     B, hq, hkv, D = cfg["batch"], cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    # the same sequences (same seed, same drawn lengths), one layer, on the host
     case = workloads.paged_case(**{**cfg, "layers": 1, "pool_pages": None})
     threads = oracle.max_threads()
     ctx = [int(t) for t in case.ctx_lens]
@@ -824,16 +866,18 @@ def main_reference(args):
     sec = time.perf_counter() - t
     ms = sec * 1e3 / args.steps
     gbs = per_layer / (ms * 1e-3) / 1e9
+    sample = (f"one of {cfg['layers']} layers per step: {B} sequences x {hq} heads, "
+              f"{sum(ctx)} cached tokens (the oracle's decode)")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), fp16)",
-        "config": {"workload": f"{HEADLINE}: one layer (8 sequences x 32 heads x 4096 "
-                               "tokens) of the decode step per step, float64 oracle"},
+        "vs_baseline": None, "dtype": "f64",
+        "data": f"synthetic (seeded N(0,1), {cfg['dtype']})",
+        "config": {"workload": describe(HEADLINE, cfg) + "; one layer per step, float64 "
+                                                         "oracle"},
         "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle",
-                         "sample": "one of 32 layers per step (the oracle's decode)"},
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -841,9 +885,10 @@ def main_reference(args):
 
 
 def ncu_case(args):
-    """A small launch sequence for ncu captures: one layer of the headline
-    workload (537 MB of KV, above L2) decoded `--steps` times after `--warmup`
-    calls, or the chunked-prefill workload.  Prints nothing to measure."""
+    """A small launch sequence for ncu captures: one layer of a decode
+    workload (the ragged GQA batch: 1.1 GB of KV; the LLaMA-shaped one: 537
+    MB; both above L2) decoded `--steps` times after `--warmup` calls, or one
+    of the other kernels' workloads.  Prints nothing to measure."""
     import torch
     import paged_kv_cache_171_gb300 as pa
     from paged_kv_cache_171_gb300 import build as pa_build
@@ -882,7 +927,7 @@ def ncu_case(args):
         for _ in range(args.warmup + args.steps):
             pa.pa_copy_pages(kc, vc, src, dst, 4096, 8, 128, 16, 8192, pa.BF16)
     else:
-        name = {"decode": HEADLINE, "decode_gqa8": "gqa8_b4_ctx32k",
+        name = {"decode": "llama7b_b8_ctx4096", "decode_gqa8": "gqa8_b4_ctx32k",
                 "decode_gqa4": "gqa4_b64_ragged", "decode_mha_small": "mha_b1_ctx512"}[
                     args.ncu_case]
         over = {"layers": 1, "pool_pages": None}
@@ -902,7 +947,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only-headline", action="store_true",
-                    help="skip the other workloads (ragged GQA, 32k split-K, prefill)")
+                    help="skip the second decode step and the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", choices=["decode", "decode_gqa8", "decode_gqa4",
                                            "decode_mha_small", "verify", "window", "topm",

@@ -16,8 +16,9 @@
 //   S_x   = Q_x K_j^T          tcgen05.mma M=128 N=128 K=head_dim, operands in
 //                              shared memory, accumulator in TMEM
 //   softmax                    one thread per row, all 128 keys of the tile
-//   P_x   -> TMEM              written over S_x as two 16-bit terms (head +
-//                              remainder) so the weights keep ~16 bits
+//   P_x   -> TMEM              written over S_x as one 16-bit term, or as
+//                              two (head + remainder, ~16 bits) where the
+//                              rounding of one term could matter (below)
 //   O_x  += P_x V_j            tcgen05.mma with A in TMEM, B in shared memory
 // The tensor pipe alternates between the two row tiles: while tile A's
 // softmax runs it computes P_B V_j and S_B for the next key tile, and the
@@ -50,12 +51,29 @@
 // tile, stage): each is used every lcm(2, stages) tiles by one waiter, in
 // order, and its phase parity stays exact.
 //
+// One or two terms of P.  Rounding a weight p to 16 bits changes it by at
+// most 2^-9 p (bf16), and the output row by sum_t w_t d_t v_t (w = p / l,
+// |d_t| <= 2^-9): on short or peaked rows that can exceed the 2e-3 absolute
+// bound, so there P keeps a remainder term.  A row tile's key tile j takes
+// one term when, in every row, the tile's largest weight is below 1/16 of
+// the weight l already accumulated over the tiles before it.  Then
+// sum over such tiles of sum_t w_t^2 <= max_j (pmax_j / l) <= 1/16, and the
+// rounding error of the single-term tiles has an rms of at most
+// 2^-9 / sqrt(3) * rms(v) / 4.  The first tile of every row tile (l = 0)
+// and any tile that holds a new dominant key take two terms.  The
+// softmax warpgroup votes per key tile (a named barrier every warp reaches,
+// failed or not) and tells the MMA warp, which then issues the remainder's
+// P V MMAs or not.  Long diffuse rows take one term on most tiles: half the
+// P V MMAs and half the P stores to tensor memory.
+//
 // Split rows.  When an interleaved tile has at most 64 real rows, rows
 // r + 64 of Q repeat rows r, so lanes r and r + 64 of S hold the same scores
 // and their softmax threads compute the same weights.  Lane r writes the head
 // term of P and lane r + 64 the remainder, into the same 64 columns: one
 // P V pass over 128 keys (8 MMAs, not 16) accumulates both, and the row's
 // output is the sum of O's lanes r and r + 64.
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_tcgen05.cuh"
@@ -106,7 +124,9 @@ struct TcSmem {
   static constexpr int kK0 = kQ + 2 * kQBytes;
   static constexpr int kV0 = kK0 + kKStages * kKVBytes;
   static constexpr int kBars = kV0 + kVStages * kKVBytes;
-  static constexpr int kSlot = kBars + 48 * 8;  // TMEM address, abort flag
+  // TMEM address, abort flag, then the P mode of row tiles A and B (1: one
+  // term) for the key tile their softmax handed over last
+  static constexpr int kSlot = kBars + 48 * 8;
   static constexpr int kML = kSlot + 16;        // interleaved: B's (m, l) per row
   static constexpr int kBytes = kML + kRows * 8;
   // Interleaved key tiles: Q_A only, then the K and V rings.
@@ -311,7 +331,8 @@ __device__ __forceinline__ void load_tiles(bool is_v, const CUtensorMap *map, ui
 // j-th key tile of row tile x is t = 2 j + x and both tiles read Q_A.
 template <int D, bool BF16, bool IL, bool SR>
 __device__ __forceinline__ void mma_tiles(int x, uint32_t sb, uint32_t tmem, const TcWork &w,
-                                          int *status, volatile int *abort_flag, int lane) {
+                                          int *status, volatile int *abort_flag,
+                                          const volatile int *mode_x, int lane) {
   using L = TcSmem<D>;
   constexpr int SK = IL ? L::kKStagesIl : L::kKStages, SV = IL ? L::kVStagesIl : L::kVStages;
   const Ring<IL> rk{SK}, rv{SV};
@@ -345,11 +366,12 @@ __device__ __forceinline__ void mma_tiles(int x, uint32_t sb, uint32_t tmem, con
   };
   // O_x += P_x[:, keys of half h] V_t[keys of half h].  P_x in TMEM: head
   // terms in columns 0-63 (two keys per column), remainders in 64-127.
-  auto pv_mma = [&](int j, int t, int h) {  // the j-th key tile of x is t
+  // Split rows: the remainders are in rows 64-127 of the same columns, so
+  // one pass; else one or two passes as the softmax decided for the tile.
+  auto pv_mma = [&](int j, int t, int h, int n_ph) {  // the j-th key tile of x is t
     if (lane == 0) {
       const uint64_t dv = dv0 + static_cast<uint64_t>(((t % SV) * L::kKVBytes) >> 4);
       const uint32_t pa = tSx + 32 * h;
-      constexpr int n_ph = SR ? 1 : 2;  // split rows: the remainders are in rows 64-127
 #pragma unroll
       for (int ph = 0; ph < 2; ++ph) {
         if (ph >= n_ph) break;
@@ -375,15 +397,20 @@ __device__ __forceinline__ void mma_tiles(int x, uint32_t sb, uint32_t tmem, con
   }
   for (int j = 0; j < nx && ok; ++j) {
     const int t = tx + kStep * j;
+    int n_ph = 1;
     for (int h = 0; h < 2 && ok; ++h) {
       if (!(ok = warp_wait(bar(kBarP + 2 * x + h), j & 1, abort_flag))) break;
       if (h == 0) {
+        // written before the softmax's first hand-off of this tile (the
+        // barrier's acquire makes it visible); rewritten only after S_x of
+        // a later tile, which is issued below
+        if (!SR) n_ph = *mode_x ? 1 : 2;
         ok = (t == n - 1 && cleared) ? warp_wait(bar(kBarVZ), 0, abort_flag)
                                      : warp_wait(bar(kBarV + rv.full(t)), rv.parity(t), abort_flag);
         if (!ok) break;
       }
       tc::fence_after_sync();
-      pv_mma(j, t, h);
+      pv_mma(j, t, h, n_ph);
     }
     const int tn = t + kStep;
     if (ok && j + 1 < nx &&
@@ -417,6 +444,19 @@ __device__ __forceinline__ bool softmax_pair_sync_any(bool c) {
 __device__ __forceinline__ void softmax_group_sync() {
   asm volatile("bar.sync 2, 128;" ::: "memory");
 }
+// Barrier 3 + x joins softmax warpgroup x (128 threads) and returns whether
+// every thread passed true.
+template <int X>
+__device__ __forceinline__ bool softmax_group_all(bool c) {
+  uint32_t all;
+  asm volatile(
+      "{\n\t.reg .pred q, p;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(all)
+      : "r"(static_cast<uint32_t>(c)), "n"(3 + X)
+      : "memory");
+  return all != 0;
+}
 
 // Softmax warpgroup x (warps 4 + 4 x .. 7 + 4 x): lane l of warp w owns TMEM
 // lane r = 32 (w % 4) + l of row tile x, i.e. row rr = r (split rows:
@@ -424,8 +464,8 @@ __device__ __forceinline__ void softmax_group_sync() {
 template <int D, int GT, bool BF16, bool IL, bool SR>
 __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const TcParams &p,
                                               const TcWork &w, volatile int *abort_flag,
-                                              float *ml, float *scratch, int x, int warp,
-                                              int lane) {
+                                              volatile int *mode_x, float *ml, float *scratch,
+                                              int x, int warp, int lane) {
   using L = TcSmem<D>;
   auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
   const int r = ((warp & 3) << 5) + lane, rr = SR ? (r & 63) : r;
@@ -444,7 +484,14 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
   bool bad = false;
   float m = -INFINITY;
   float2 lp = make_float2(0.f, 0.f);  // running sums of the even and odd keys
-  for (int j = 0; j < nt; ++j) {
+  // The per-key-tile vote (one term of P or two) is a named barrier of the
+  // warpgroup: every warp reaches it once per key tile.  A warp whose wait
+  // failed leaves the loop and casts its remaining votes afterwards.
+  auto vote = [&](bool fine) {
+    return x == 0 ? softmax_group_all<0>(fine) : softmax_group_all<1>(fine);
+  };
+  int j = 0;
+  for (; j < nt; ++j) {
     // ping-pong: wait for the other tile's turn before this one (where the
     // other tile has that many key tiles)
     const int jo = j - 1 + x;
@@ -491,64 +538,92 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
       m = mn;
       lp = __fmul2_rn(lp, make_float2(corr, corr));
     }
+    // ---- one term of P for this key tile if, in every row of the tile, its
+    // largest weight 2^(cand - m) is below 1/16 of the weight of the earlier
+    // tiles (NaN while m = -inf: two terms)
+    bool one = false;
+    if constexpr (!SR) {
+      one = vote(16.f * ex2(cand - m) < lp.x + lp.y);
+      if ((warp & 3) == 0 && lane == 0) *mode_x = one ? 1 : 0;
+    }
     const float nm = m == -INFINITY ? 0.f : -m;  // nothing seen yet: weights are 0
     const float2 qs2 = make_float2(qs, qs), nm2 = make_float2(nm, nm);
 
-    // ---- P = 2^(s qs - m) as head + remainder, over the S columns; each
-    // half of the keys is handed to the MMA warp as soon as it is written
+    // ---- P = 2^(s qs - m), one term or head + remainder, over the S
+    // columns; each half of the keys is handed to the MMA warp as soon as it
+    // is written.  Kind 0: head + remainder, 1: one term, 2: split rows (the
+    // warps of rows 0-63 store the head term, those of rows 64-127 the
+    // remainder, into the same columns).  Each kind is its own unrolled loop.
+    auto tile_p = [&](auto kind) {
+      constexpr int K = decltype(kind)::value;
 #pragma unroll
-    for (int ch = 0; ch < kKeys / 32; ++ch) {  // keys 32 ch .. 32 ch + 31
-      uint32_t phi[16], plo[16];
-      // packed fp32x2 arithmetic: one instruction per key pair; split rows:
-      // the warps of rows 0-63 store only the head term, so only the
-      // remainder warps (rows 64-127) compute the remainder
-      auto head = [&](int k) {
-        const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[32 * ch + 2 * k]),
-                                                __uint_as_float(s[32 * ch + 2 * k + 1])),
-                                    qs2, nm2);
-        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-        lp = __fadd2_rn(lp, pp);
-        phi[k] = pack2<BF16>(pp.x, pp.y);
-        return pp;
-      };
-      if (!SR || rem) {
+      for (int ch = 0; ch < kKeys / 32; ++ch) {  // keys 32 ch .. 32 ch + 31
+        uint32_t phi[16], plo[16];
+        // packed fp32x2 arithmetic: one instruction per key pair
+        auto head = [&](int k) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[32 * ch + 2 * k]),
+                                                  __uint_as_float(s[32 * ch + 2 * k + 1])),
+                                      qs2, nm2);
+          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+          lp = __fadd2_rn(lp, pp);
+          phi[k] = pack2<BF16>(pp.x, pp.y);
+          return pp;
+        };
+        auto head_and_rem = [&] {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float2 pp = head(k);
-          const float2 d = __ffma2_rn(unpack2<BF16>(phi[k]), make_float2(-1.f, -1.f), pp);
-          plo[k] = pack2<BF16>(d.x, d.y);  // the remainder p - head, exact before rounding
+          for (int k = 0; k < 16; ++k) {
+            const float2 pp = head(k);
+            const float2 d = __ffma2_rn(unpack2<BF16>(phi[k]), make_float2(-1.f, -1.f), pp);
+            plo[k] = pack2<BF16>(d.x, d.y);  // the remainder p - head, exact before rounding
+          }
+        };
+        if constexpr (K == 2) {
+          if (rem) {
+            head_and_rem();
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) head(k);
+          }
+          tc::st16(tSx + 16 * ch, rem ? plo : phi);
+        } else if constexpr (K == 1) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) head(k);
+          tc::st16(tSx + 16 * ch, phi);
+        } else {
+          head_and_rem();
+          tc::st16(tSx + 16 * ch, phi);
+          tc::st16(tSx + 64 + 16 * ch, plo);
         }
-      } else {
+        if (ch == 1 && j > 0 && __any_sync(kFull, need)) {
+          // the max moved: rescale this row of O_x before the first P V of
+          // this tile (P_x V_{j-1} has completed: S_x was issued after it)
 #pragma unroll
-        for (int k = 0; k < 16; ++k) head(k);
-      }
-      if (!SR) {
-        tc::st16(tSx + 16 * ch, phi);
-        tc::st16(tSx + 64 + 16 * ch, plo);
-      } else {
-        tc::st16(tSx + 16 * ch, rem ? plo : phi);
-      }
-      if (ch == 1 && j > 0 && __any_sync(kFull, need)) {
-        // the max moved: rescale this row of O_x before the first P V of
-        // this tile (P_x V_{j-1} has completed: S_x was issued after it)
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t o[32];
+            tc::ld32(tOx + cb * 32, o);
+            tc::wait_ld();
 #pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t o[32];
-          tc::ld32(tOx + cb * 32, o);
-          tc::wait_ld();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
-          tc::st32(tOx + cb * 32, o);
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
+            tc::st32(tOx + cb * 32, o);
+          }
+        }
+        if (ch & 1) {
+          tc::wait_st();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarP + 2 * x + (ch >> 1)));  // one arrival per warp
         }
       }
-      if (ch & 1) {
-        tc::wait_st();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarP + 2 * x + (ch >> 1)));  // one arrival per warp
-      }
-    }
+    };
+    if constexpr (SR)
+      tile_p(std::integral_constant<int, 2>{});
+    else if (one)
+      tile_p(std::integral_constant<int, 1>{});
+    else
+      tile_p(std::integral_constant<int, 0>{});
   }
+  if constexpr (!SR)
+    for (; j < nt; ++j) vote(false);  // the votes of the tiles a failed warp left
   tc::wait_st();
   if (nt == 0) return;
   if (!bad) bad = !warp_wait(bar(kBarO + x), 0, abort_flag);
@@ -693,11 +768,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   w.sr = w.il && w.nq[0] * GT <= kRows / 2;
   const int n_pages = (ctx + p.n_new + 15) >> 4;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kSlot + 4);
+  volatile int *mode = reinterpret_cast<volatile int *>(smem + L::kSlot + 8);  // [2]
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i)
       mbar_init(bar(i), (i >= kBarP && i < kBarP + 4) ? 4 : 1);
     *abort_flag = 0;
+    mode[0] = mode[1] = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -745,25 +822,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_tiles<D, false>(is_v, is_v ? &vmap : &kmap, sb, bt_row, n_pages, w, p.num_pages,
                            p.n_kv_heads * 16, p.status, abort_flag, lane);
   } else if (warp < 2) {
+    const volatile int *mode_x = mode + warp;
     if (w.sr)
-      mma_tiles<D, BF16, true, true>(warp, sb, tmem, w, p.status, abort_flag, lane);
+      mma_tiles<D, BF16, true, true>(warp, sb, tmem, w, p.status, abort_flag, mode_x,
+                                        lane);
     else if (w.il)
-      mma_tiles<D, BF16, true, false>(warp, sb, tmem, w, p.status, abort_flag, lane);
+      mma_tiles<D, BF16, true, false>(warp, sb, tmem, w, p.status, abort_flag, mode_x,
+                                        lane);
     else
-      mma_tiles<D, BF16, false, false>(warp, sb, tmem, w, p.status, abort_flag, lane);
+      mma_tiles<D, BF16, false, false>(warp, sb, tmem, w, p.status, abort_flag, mode_x,
+                                        lane);
   } else if (warp >= kSoftmaxWarp0) {
     float *ml = reinterpret_cast<float *>(smem + L::kML);
     float *scratch = reinterpret_cast<float *>(smem + L::kQ);
     const int x = (warp - kSoftmaxWarp0) >> 2;
     if (w.sr)
-      softmax_tiles<D, GT, BF16, true, true>(sb, tmem, p, w, abort_flag, ml, scratch, x, warp,
-                                             lane);
+      softmax_tiles<D, GT, BF16, true, true>(sb, tmem, p, w, abort_flag, mode + x, ml, scratch,
+                                             x, warp, lane);
     else if (w.il)
-      softmax_tiles<D, GT, BF16, true, false>(sb, tmem, p, w, abort_flag, ml, scratch, x, warp,
-                                              lane);
+      softmax_tiles<D, GT, BF16, true, false>(sb, tmem, p, w, abort_flag, mode + x, ml, scratch,
+                                              x, warp, lane);
     else
-      softmax_tiles<D, GT, BF16, false, false>(sb, tmem, p, w, abort_flag, ml, scratch, x,
-                                               warp, lane);
+      softmax_tiles<D, GT, BF16, false, false>(sb, tmem, p, w, abort_flag, mode + x, ml,
+                                               scratch, x, warp, lane);
   }
   tc::fence_before_sync();
   __syncthreads();

@@ -11,7 +11,8 @@ import torch
 import oracle
 import paged_kv_cache_171_gb300 as pa
 import workloads
-from tests.gpu_support import assert_close, compact_host_copy, to_device
+from tests.gpu_support import assert_close, to_device
+from workloads import compact_host_copy
 
 pytestmark = pytest.mark.gpu
 

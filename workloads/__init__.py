@@ -183,3 +183,28 @@ def new_tokens(n_tok: int, n_kv_heads: int, head_dim: int, dtype: str,
     _fill_normal(k, gen)
     _fill_normal(v, gen)
     return k, v
+
+
+def compact_host_copy(case, layer, seqs, extra_tokens=0):
+    """Host tensors (q, k, v, table, ctx) holding only sequences `seqs` of
+    `layer`, with their pages copied in logical order (table = identity per
+    sequence).  extra_tokens counts tokens held beyond ctx_lens (prefill)."""
+    ctx = case.ctx_lens.detach().cpu().to(torch.int64)
+    bt = case.block_table[layer].detach().cpu()
+    ids, rows, pos = [], [], 0
+    nb = [int((int(ctx[s]) + extra_tokens + 15) // 16) for s in seqs]
+    mb = max(1, max(nb))
+    table = torch.full((len(seqs), mb), -1, dtype=torch.int32)
+    for i, s in enumerate(seqs):
+        pages = bt[s, :nb[i]].to(torch.int64)
+        ids.append(pages)
+        table[i, :nb[i]] = torch.arange(pos, pos + nb[i], dtype=torch.int32)
+        pos += nb[i]
+    idx = torch.cat(ids) if ids else torch.zeros(0, dtype=torch.int64)
+    idx_dev = idx.to(case.k_cache.device)
+    k = case.k_cache.index_select(0, idx_dev).cpu()
+    v = case.v_cache.index_select(0, idx_dev).cpu()
+    sel = torch.as_tensor(seqs, dtype=torch.int64, device=case.q.device)
+    q = case.q[layer].index_select(0, sel).cpu()
+    c = ctx[list(seqs)].to(torch.int32)
+    return q, k, v, table, c

@@ -388,9 +388,11 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
  * (pa_decode_workspace_size() > 16 MiB; about batch * n_q_heads * n_parts *
  * (head_dim + 4) * 4 bytes above that) returns PA_ERR_SCRATCH_LIMIT and
  * launches nothing.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call shares the one array and leaves its contents behind;
+ * The first call in a CUDA context looks up the array's device address (with
+ * that context's device current) and caches it under the context's unique
+ * id, so a device reset or a second context on the same device looks it up
+ * again; make that first call before any stream capture.  Every call shares
+ * the one array and leaves its contents behind;
  * nothing in it needs to start at zero (each call clears its own arrival
  * counters on the stream first).  Calls that overlap on the GPU (two
  * streams, or two host threads, with split-K plans) race on the array: the

@@ -10,17 +10,40 @@ namespace pa {
 // One status word per device: the first data-dependent error any kernel saw.
 __device__ int g_status_word;
 
-int *device_status(int device) {
-  static std::mutex mu;
-  static int *addr[64] = {};
-  if (device < 0 || device >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[device]) {
+uint64_t current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext *);
+  using GetId = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    addr[device] = static_cast<int *>(p);
-  }
-  return addr[device];
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;  // nothing cached: every lookup is made again
+  return id;
+}
+
+int *device_status() {
+  static ContextCache<int *> cache;
+  int *addr = nullptr;
+  if (cache.get(current_context_id(), &addr)) return addr;
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+  cache.put(current_context_id(), static_cast<int *>(p));  // the lookup made one current
+  return static_cast<int *>(p);
 }
 
 namespace {
@@ -141,9 +164,7 @@ int check_common(int n_q_heads, int n_kv_heads, int head_dim, int page_size,
 }
 
 int current_status_ptr(int **status) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-  *status = device_status(dev);
+  *status = device_status();
   return *status ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -159,8 +180,10 @@ int sm_count() {
 // partition count.  Automatic mode, with R = resident CTAs (2 per SM) and
 // I = batch * kv heads * head tiles (CTAs of a single pass):
 //   I <  3R/4: cut sequences into about R / I equal partitions, so that one
-//              wave of CTAs keeps enough copies in flight, of at most 256
-//              pages each;
+//              wave of CTAs keeps enough copies in flight, of 2 to 256 pages
+//              each (a small call -- a few MB of KV -- is latency-bound: its
+//              short partitions, owned by single warps below, put every page
+//              in flight at once, so the call takes one HBM round trip);
 //   I <  R   : a single pass (one wave, no merge);
 //   I >= R   : cut into 4 partitions of >= 32 pages, so that one long
 //              sequence of a ragged batch cannot make a tail of its own.
@@ -177,7 +200,12 @@ int decode_plan(int batch, int n_q_heads, int n_kv_heads, int max_blocks,
     if (items * 4 < resident * 3) {
       const int64_t want = resident / items > 1 ? resident / items : 1;
       int64_t per = (max_blocks + want - 1) / want;
-      if (per < 16) per = 16;
+      if (per <= 32) {
+        // short partitions go to single warps (below): about `want` CTA
+        // slots per item is kDecodeWarps partitions per slot
+        per = (max_blocks + want * kDecodeWarps - 1) / (want * kDecodeWarps);
+        if (per < 2) per = 2;
+      }
       if (per > 256) per = 256;  // longer ranges leave a slow tail (measured at 32k)
       pp = static_cast<int>(per);
     } else if (items < resident) {

@@ -908,15 +908,8 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   const bool split = gx > 1;  // else one CTA per (sequence, head tile)
   auto kern = split ? decode_kernel<D, GT, BF16, NW, S, MMA, true>
                     : decode_kernel<D, GT, BF16, NW, S, MMA, false>;
-  static uint64_t attr_set[2] = {0, 0};  // one bit per device ordinal and variant
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return PA_ERR_CUDA;
-  if (!(attr_set[split] >> dev & 1)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kAlloc) != cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set[split] |= uint64_t(1) << dev;
-  }
+  static ContextCache<bool> smem_set[2];  // per variant: contexts where the limit is set
+  if (set_smem_limit(kern, L::kAlloc, smem_set[split]) != PA_OK) return PA_ERR_CUDA;
   CUtensorMap kmap, vmap;
   const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.n_kv_heads * 16;
   if (make_rows_map(&kmap, a.k_cache, rows, D, 16) != PA_OK) return PA_ERR_CUDA;

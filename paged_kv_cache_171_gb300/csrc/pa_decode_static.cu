@@ -8,8 +8,6 @@
 // cudaFree may synchronise the whole device, or a caller that only speaks the
 // C ABI and has no allocator at hand.  Such callers still pass q, the caches,
 // the tables and the output; only the scratch comes from here.
-#include <mutex>
-
 #include "pa_internal.h"
 
 namespace {
@@ -20,19 +18,17 @@ constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
-// Device address of the array, looked up once per device with that device
-// current (the symbol's name in host code is only a stand-in).
-void *scratch_address(int device) {
-  static std::mutex mu;
-  static void *addr[64] = {};
-  if (device < 0 || device >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[device]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
-    addr[device] = p;
-  }
-  return addr[device];
+// Device address of the array in the current context (the symbol's name in
+// host code is only a stand-in).  Looked up once per CUDA context and cached
+// under the context's unique id, so a device reset or another context on
+// the same device never sees a stale address.
+void *scratch_address() {
+  static pa::ContextCache<void *> cache;
+  void *addr = nullptr;
+  if (cache.get(pa::current_context_id(), &addr)) return addr;
+  if (cudaGetSymbolAddress(&addr, g_decode_scratch) != cudaSuccess) return nullptr;
+  cache.put(pa::current_context_id(), addr);  // the lookup made a context current
+  return addr;
 }
 
 }  // namespace
@@ -55,9 +51,7 @@ extern "C" int pa_decode_static_workspace(
   if (need > kStaticScratchBytes) return PA_ERR_SCRATCH_LIMIT;
   void *scratch = nullptr;
   if (need > 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-    scratch = scratch_address(dev);
+    scratch = scratch_address();
     if (!scratch) return PA_ERR_CUDA;
   }
   // Every partial state the merge reads is written by the same call first,

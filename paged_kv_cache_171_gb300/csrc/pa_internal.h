@@ -7,9 +7,63 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "pa.h"
 
 namespace pa {
+
+// Unique id of the calling thread's current CUDA context, or 0 while none is
+// current.  CUDA never gives two contexts of one process the same id, so
+// values cached under it go stale neither after cudaDeviceReset (the next
+// primary context has a new id) nor when a second context is made current on
+// the same device.
+uint64_t current_context_id();
+
+// Values computed once per CUDA context (a symbol's device address, whether a
+// kernel attribute is set), keyed by current_context_id().  Thread-safe.
+template <class T>
+class ContextCache {
+ public:
+  bool get(uint64_t ctx, T *out) {
+    if (ctx == 0) return false;
+    std::lock_guard<std::mutex> lock(mu_);
+    for (const auto &e : entries_)
+      if (e.first == ctx) {
+        *out = e.second;
+        return true;
+      }
+    return false;
+  }
+  void put(uint64_t ctx, T value) {
+    if (ctx == 0) return;
+    std::lock_guard<std::mutex> lock(mu_);
+    for (auto &e : entries_)
+      if (e.first == ctx) {
+        e.second = value;
+        return;
+      }
+    entries_.emplace_back(ctx, value);
+  }
+
+ private:
+  std::mutex mu_;
+  std::vector<std::pair<uint64_t, T>> entries_;
+};
+
+// Raises `kern`'s dynamic shared-memory limit to `bytes`, once per context.
+template <class K>
+int set_smem_limit(K *kern, int bytes, ContextCache<bool> &done) {
+  bool set = false;
+  if (done.get(current_context_id(), &set)) return PA_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  done.put(current_context_id(), true);  // the call above made a context current
+  return PA_OK;
+}
 
 constexpr int kPageSize = 16;  // tokens per page (the only one supported)
 
@@ -107,8 +161,9 @@ int launch_merge_rows(const float *partials, const int32_t *ctx_lens, float *out
 
 int launch_prefill(const PrefillLaunch &a, cudaStream_t stream);
 
-// Device address of this device's status word (looked up once per device).
-int *device_status(int device);
+// Device address of the current context's status word (looked up once per
+// context), or nullptr if the lookup fails.
+int *device_status();
 
 // Tiled tensor map over a [rows][head_dim] 16-bit matrix, box {64, box_rows},
 // 128-byte swizzle.  Returns PA_OK or PA_ERR_CUDA.

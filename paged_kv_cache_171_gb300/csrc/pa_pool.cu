@@ -166,9 +166,7 @@ int pa_copy_pages(void *k_cache, void *v_cache, const int32_t *src, const int32_
   if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
     return PA_ERR_ALIGN;
   if (n == 0) return PA_OK;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-  int *status = device_status(dev);
+  int *status = device_status();
   if (!status) return PA_ERR_CUDA;
   const size_t page_vecs = static_cast<size_t>(n_kv_heads) * page_size * head_dim * 2 / 16;
   if (launch_pdl(copy_pages_kernel, dim3(2 * n), dim3(256), 0,

@@ -60,11 +60,14 @@
 // sum over such tiles of sum_t w_t^2 <= max_j (pmax_j / l) <= 1/16, and the
 // rounding error of the single-term tiles has an rms of at most
 // 2^-9 / sqrt(3) * rms(v) / 4.  The first tile of every row tile (l = 0)
-// and any tile that holds a new dominant key take two terms.  The
-// softmax warpgroup votes per key tile (a named barrier every warp reaches,
-// failed or not) and tells the MMA warp, which then issues the remainder's
-// P V MMAs or not.  Long diffuse rows take one term on most tiles: half the
-// P V MMAs and half the P stores to tensor memory.
+// and any tile that holds a new dominant key take two terms.  The four
+// warps of a softmax warpgroup vote per key tile: each posts its warp's
+// verdict and arrives on an mbarrier after the head terms of its first 32
+// keys, and reads the four verdicts after those of the first 64, so the
+// vote's latency hides behind work that both modes share.  One thread tells the
+// MMA warp, which then issues the remainder's P V MMAs or not.  Long diffuse
+// rows take one term on most tiles: half the P V MMAs and half the P stores
+// to tensor memory.
 //
 // Split rows.  When an interleaved tile has at most 64 real rows, rows
 // r + 64 of Q repeat rows r, so lanes r and r + 64 of S hold the same scores
@@ -128,7 +131,8 @@ struct TcSmem {
   // term) for the key tile their softmax handed over last
   static constexpr int kSlot = kBars + 48 * 8;
   static constexpr int kML = kSlot + 16;        // interleaved: B's (m, l) per row
-  static constexpr int kBytes = kML + kRows * 8;
+  static constexpr int kVote = kML + kRows * 8;  // per softmax warp: one term fits its rows
+  static constexpr int kBytes = kVote + 8 * 4;
   // Interleaved key tiles: Q_A only, then the K and V rings.
   static constexpr int kKStagesIl = D == 128 ? 3 : 4;
   static constexpr int kVStagesIl = D == 128 ? 3 : 4;
@@ -153,7 +157,9 @@ enum {
   kBarO = 38,       // the last P_x V done (commit, once), per row tile
   kBarVZ = 40,      // the last V tile's rows past the final key are cleared
   kBarDrain = 41,   // an MMA warp's own drain on its failure path, per row tile
-  kNumBars = 43
+  kBarVote = 43,    // the four warps of softmax warpgroup x have voted (one
+                    // arrival each), per row tile
+  kNumBars = 45
 };
 static_assert(kNumBars <= 48, "barrier space");
 
@@ -444,28 +450,15 @@ __device__ __forceinline__ bool softmax_pair_sync_any(bool c) {
 __device__ __forceinline__ void softmax_group_sync() {
   asm volatile("bar.sync 2, 128;" ::: "memory");
 }
-// Barrier 3 + x joins softmax warpgroup x (128 threads) and returns whether
-// every thread passed true.
-template <int X>
-__device__ __forceinline__ bool softmax_group_all(bool c) {
-  uint32_t all;
-  asm volatile(
-      "{\n\t.reg .pred q, p;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, %2, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(all)
-      : "r"(static_cast<uint32_t>(c)), "n"(3 + X)
-      : "memory");
-  return all != 0;
-}
-
 // Softmax warpgroup x (warps 4 + 4 x .. 7 + 4 x): lane l of warp w owns TMEM
 // lane r = 32 (w % 4) + l of row tile x, i.e. row rr = r (split rows:
 // r mod 64): query qx[x] + rr / GT, head hbase + rr % GT.
 template <int D, int GT, bool BF16, bool IL, bool SR>
 __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const TcParams &p,
                                               const TcWork &w, volatile int *abort_flag,
-                                              volatile int *mode_x, float *ml, float *scratch,
-                                              int x, int warp, int lane) {
+                                              volatile int *mode_x, volatile int *votes,
+                                              float *ml, float *scratch, int x, int warp,
+                                              int lane) {
   using L = TcSmem<D>;
   auto bar = [&](int i) { return sb + L::kBars + 8 * i; };
   const int r = ((warp & 3) << 5) + lane, rr = SR ? (r & 63) : r;
@@ -484,14 +477,7 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
   bool bad = false;
   float m = -INFINITY;
   float2 lp = make_float2(0.f, 0.f);  // running sums of the even and odd keys
-  // The per-key-tile vote (one term of P or two) is a named barrier of the
-  // warpgroup: every warp reaches it once per key tile.  A warp whose wait
-  // failed leaves the loop and casts its remaining votes afterwards.
-  auto vote = [&](bool fine) {
-    return x == 0 ? softmax_group_all<0>(fine) : softmax_group_all<1>(fine);
-  };
-  int j = 0;
-  for (; j < nt; ++j) {
+  for (int j = 0; j < nt; ++j) {
     // ping-pong: wait for the other tile's turn before this one (where the
     // other tile has that many key tiles)
     const int jo = j - 1 + x;
@@ -538,92 +524,132 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
       m = mn;
       lp = __fmul2_rn(lp, make_float2(corr, corr));
     }
-    // ---- one term of P for this key tile if, in every row of the tile, its
+    // ---- this row's verdict: one term of P for this key tile if the tile's
     // largest weight 2^(cand - m) is below 1/16 of the weight of the earlier
-    // tiles (NaN while m = -inf: two terms)
-    bool one = false;
-    if constexpr (!SR) {
-      one = vote(16.f * ex2(cand - m) < lp.x + lp.y);
-      if ((warp & 3) == 0 && lane == 0) *mode_x = one ? 1 : 0;
-    }
+    // tiles (NaN while m = -inf: two terms); the warpgroup votes below
+    const bool fine = 16.f * ex2(cand - m) < lp.x + lp.y;
     const float nm = m == -INFINITY ? 0.f : -m;  // nothing seen yet: weights are 0
     const float2 qs2 = make_float2(qs, qs), nm2 = make_float2(nm, nm);
 
-    // ---- P = 2^(s qs - m), one term or head + remainder, over the S
-    // columns; each half of the keys is handed to the MMA warp as soon as it
+    auto head = [&](int ch, int k, uint32_t &hi) {  // packed fp32x2: one instruction per pair
+      const float2 e = __ffma2_rn(make_float2(__uint_as_float(s[32 * ch + 2 * k]),
+                                              __uint_as_float(s[32 * ch + 2 * k + 1])),
+                                  qs2, nm2);
+      const float2 pp = make_float2(ex2(e.x), ex2(e.y));
+      lp = __fadd2_rn(lp, pp);
+      hi = pack2<BF16>(pp.x, pp.y);
+      return pp;
+    };
+    auto rem_of = [&](float2 pp, uint32_t hi) {  // the remainder p - head, exact before rounding
+      const float2 d = __ffma2_rn(unpack2<BF16>(hi), make_float2(-1.f, -1.f), pp);
+      return pack2<BF16>(d.x, d.y);
+    };
+    // After chunk ch's stores: the O rescale (once per tile, before the
+    // first P V of the tile) and the hand-off of each 64-key half.
+    auto after_chunk = [&](int ch) {
+      if (ch == 1 && j > 0 && __any_sync(kFull, need)) {
+        // the max moved: rescale this row of O_x before the first P V of
+        // this tile (P_x V_{j-1} has completed: S_x was issued after it)
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t o[32];
+          tc::ld32(tOx + cb * 32, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
+          tc::st32(tOx + cb * 32, o);
+        }
+      }
+      if (ch & 1) {
+        tc::wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarP + 2 * x + (ch >> 1)));  // one arrival per warp
+      }
+    };
+    // ---- P = 2^(s qs - m) over the S columns, keys 32 ch .. 32 ch + 31 per
+    // chunk; each half of the keys is handed to the MMA warp as soon as it
     // is written.  Kind 0: head + remainder, 1: one term, 2: split rows (the
     // warps of rows 0-63 store the head term, those of rows 64-127 the
     // remainder, into the same columns).  Each kind is its own unrolled loop.
-    auto tile_p = [&](auto kind) {
+    auto tile_p = [&](auto kind, int ch0) {  // chunks ch0 .. 3
       constexpr int K = decltype(kind)::value;
 #pragma unroll
-      for (int ch = 0; ch < kKeys / 32; ++ch) {  // keys 32 ch .. 32 ch + 31
+      for (int ch = 0; ch < kKeys / 32; ++ch) {
+        if (ch < ch0) continue;
         uint32_t phi[16], plo[16];
-        // packed fp32x2 arithmetic: one instruction per key pair
-        auto head = [&](int k) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[32 * ch + 2 * k]),
-                                                  __uint_as_float(s[32 * ch + 2 * k + 1])),
-                                      qs2, nm2);
-          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-          lp = __fadd2_rn(lp, pp);
-          phi[k] = pack2<BF16>(pp.x, pp.y);
-          return pp;
-        };
-        auto head_and_rem = [&] {
+        if constexpr (K == 2) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float2 pp = head(k);
-            const float2 d = __ffma2_rn(unpack2<BF16>(phi[k]), make_float2(-1.f, -1.f), pp);
-            plo[k] = pack2<BF16>(d.x, d.y);  // the remainder p - head, exact before rounding
-          }
-        };
-        if constexpr (K == 2) {
-          if (rem) {
-            head_and_rem();
-          } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) head(k);
+            const float2 pp = head(ch, k, phi[k]);
+            if (rem) plo[k] = rem_of(pp, phi[k]);
           }
           tc::st16(tSx + 16 * ch, rem ? plo : phi);
         } else if constexpr (K == 1) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) head(k);
+          for (int k = 0; k < 16; ++k) head(ch, k, phi[k]);
           tc::st16(tSx + 16 * ch, phi);
         } else {
-          head_and_rem();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) plo[k] = rem_of(head(ch, k, phi[k]), phi[k]);
           tc::st16(tSx + 16 * ch, phi);
           tc::st16(tSx + 64 + 16 * ch, plo);
         }
-        if (ch == 1 && j > 0 && __any_sync(kFull, need)) {
-          // the max moved: rescale this row of O_x before the first P V of
-          // this tile (P_x V_{j-1} has completed: S_x was issued after it)
-#pragma unroll
-          for (int cb = 0; cb < D / 32; ++cb) {
-            uint32_t o[32];
-            tc::ld32(tOx + cb * 32, o);
-            tc::wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
-            tc::st32(tOx + cb * 32, o);
-          }
-        }
-        if (ch & 1) {
-          tc::wait_st();
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarP + 2 * x + (ch >> 1)));  // one arrival per warp
-        }
+        after_chunk(ch);
       }
     };
-    if constexpr (SR)
-      tile_p(std::integral_constant<int, 2>{});
-    else if (one)
-      tile_p(std::integral_constant<int, 1>{});
-    else
-      tile_p(std::integral_constant<int, 0>{});
+    if constexpr (SR) {
+      tile_p(std::integral_constant<int, 2>{}, 0);
+    } else {
+      // Keys 0-63: head terms first (both modes need them; the weights stay
+      // in s for a remainder), the warp's verdict posted after the first 32
+      // and the four verdicts read after all 64, so that neither the vote's
+      // latency nor a branch on its outcome holds up the exponentials.
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t phi[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 pp = head(ch, k, phi[k]);
+          s[32 * ch + 2 * k] = __float_as_uint(pp.x);
+          s[32 * ch + 2 * k + 1] = __float_as_uint(pp.y);
+        }
+        tc::st16(tSx + 16 * ch, phi);
+        if (ch == 0) {
+          const bool wfine = __all_sync(kFull, fine);
+          if (lane == 0) {
+            votes[4 * x + (warp & 3)] = wfine ? 1 : 0;
+            mbar_arrive(bar(kBarVote + x));
+          }
+        }
+      }
+      if (!warp_wait(bar(kBarVote + x), j & 1, abort_flag)) {
+        bad = true;
+        if (lane == 0) raise_abort(p.status, abort_flag);
+        break;
+      }
+      const bool one = votes[4 * x] & votes[4 * x + 1] & votes[4 * x + 2] & votes[4 * x + 3];
+      if ((warp & 3) == 0 && lane == 0) *mode_x = one ? 1 : 0;
+      if (!one) {  // remainders of keys 0-63 from the kept weights
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t plo[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 pp = make_float2(__uint_as_float(s[32 * ch + 2 * k]),
+                                          __uint_as_float(s[32 * ch + 2 * k + 1]));
+            plo[k] = rem_of(pp, pack2<BF16>(pp.x, pp.y));
+          }
+          tc::st16(tSx + 64 + 16 * ch, plo);
+        }
+      }
+      after_chunk(1);  // the O rescale, then keys 0-63 go to the MMA warp
+      if (one)
+        tile_p(std::integral_constant<int, 1>{}, 2);
+      else
+        tile_p(std::integral_constant<int, 0>{}, 2);
+    }
   }
-  if constexpr (!SR)
-    for (; j < nt; ++j) vote(false);  // the votes of the tiles a failed warp left
   tc::wait_st();
   if (nt == 0) return;
   if (!bad) bad = !warp_wait(bar(kBarO + x), 0, abort_flag);
@@ -769,10 +795,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_pages = (ctx + p.n_new + 15) >> 4;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kSlot + 4);
   volatile int *mode = reinterpret_cast<volatile int *>(smem + L::kSlot + 8);  // [2]
+  volatile int *votes = reinterpret_cast<volatile int *>(smem + L::kVote);     // [2][4]
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i)
-      mbar_init(bar(i), (i >= kBarP && i < kBarP + 4) ? 4 : 1);
+      mbar_init(bar(i), ((i >= kBarP && i < kBarP + 4) || i >= kBarVote) ? 4 : 1);
     *abort_flag = 0;
     mode[0] = mode[1] = 0;
     fence_mbar_init();
@@ -824,26 +851,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 2) {
     const volatile int *mode_x = mode + warp;
     if (w.sr)
-      mma_tiles<D, BF16, true, true>(warp, sb, tmem, w, p.status, abort_flag, mode_x,
-                                        lane);
+      mma_tiles<D, BF16, true, true>(warp, sb, tmem, w, p.status, abort_flag, mode_x, lane);
     else if (w.il)
-      mma_tiles<D, BF16, true, false>(warp, sb, tmem, w, p.status, abort_flag, mode_x,
-                                        lane);
+      mma_tiles<D, BF16, true, false>(warp, sb, tmem, w, p.status, abort_flag, mode_x, lane);
     else
-      mma_tiles<D, BF16, false, false>(warp, sb, tmem, w, p.status, abort_flag, mode_x,
-                                        lane);
+      mma_tiles<D, BF16, false, false>(warp, sb, tmem, w, p.status, abort_flag, mode_x, lane);
   } else if (warp >= kSoftmaxWarp0) {
     float *ml = reinterpret_cast<float *>(smem + L::kML);
     float *scratch = reinterpret_cast<float *>(smem + L::kQ);
     const int x = (warp - kSoftmaxWarp0) >> 2;
     if (w.sr)
-      softmax_tiles<D, GT, BF16, true, true>(sb, tmem, p, w, abort_flag, mode + x, ml, scratch,
-                                             x, warp, lane);
+      softmax_tiles<D, GT, BF16, true, true>(sb, tmem, p, w, abort_flag, mode + x, votes, ml,
+                                             scratch, x, warp, lane);
     else if (w.il)
-      softmax_tiles<D, GT, BF16, true, false>(sb, tmem, p, w, abort_flag, mode + x, ml, scratch,
-                                              x, warp, lane);
+      softmax_tiles<D, GT, BF16, true, false>(sb, tmem, p, w, abort_flag, mode + x, votes, ml,
+                                              scratch, x, warp, lane);
     else
-      softmax_tiles<D, GT, BF16, false, false>(sb, tmem, p, w, abort_flag, mode + x, ml,
+      softmax_tiles<D, GT, BF16, false, false>(sb, tmem, p, w, abort_flag, mode + x, votes, ml,
                                                scratch, x, warp, lane);
   }
   tc::fence_before_sync();
@@ -858,15 +882,8 @@ template <int D, int GT, bool BF16>
 int launch_tc_t(const PrefillLaunch &a, cudaStream_t stream) {
   using L = TcSmem<D>;
   auto kern = prefill_tc_kernel<D, GT, BF16>;
-  static uint64_t attr_set = 0;  // one bit per device ordinal
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return PA_ERR_CUDA;
-  if (!(attr_set >> dev & 1)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kAlloc) != cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set |= uint64_t(1) << dev;
-  }
+  static ContextCache<bool> smem_set;  // contexts where the limit is set
+  if (set_smem_limit(kern, L::kAlloc, smem_set) != PA_OK) return PA_ERR_CUDA;
   CUtensorMap kmap, vmap;
   const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.n_kv_heads * 16;
   if (make_rows_map(&kmap, a.k_cache, rows, D, 16) != PA_OK) return PA_ERR_CUDA;

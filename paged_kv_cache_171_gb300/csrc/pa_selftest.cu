@@ -27,9 +27,7 @@ __global__ void __launch_bounds__(32) wait_timeout_kernel(int *status) {
 using namespace pa;
 
 extern "C" int pa_selftest_wait_timeout(pa_stream_t stream) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-  int *status = device_status(dev);
+  int *status = device_status();
   if (!status) return PA_ERR_CUDA;
   wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -2,9 +2,10 @@
 allocate device memory (a host framework that owns every allocation, a
 latency-critical path where cudaMalloc may synchronise the device, a caller
 with only the C ABI and no allocator).  Its split-K scratch lives in the
-library's fixed 16 MiB device array.  Checked through the C ABI against
-pa_decode with a caller-allocated workspace, on two calls in a row (so the
-second sees the first call's leftovers in the shared array).
+library's fixed 16 MiB device array.  Checked through the C ABI, on two calls
+in a row that both use split-K plans (so the second sees the first call's
+leftovers in the shared array), against the float64 oracle and against
+pa_decode with a caller-allocated workspace.
 
 This file is named to be collected last."""
 import ctypes
@@ -13,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_171_gb300 as pa
 import workloads
 from tests.gpu_support import assert_close, to_device
@@ -62,26 +64,31 @@ def _static(L, case, part):
     return out
 
 
-def test_static_workspace_matches_pa_decode_on_two_calls_in_a_row(L):
+def test_static_workspace_matches_oracle_and_pa_decode_on_two_calls_in_a_row(L):
     # call 1: long GQA-8 contexts, 512-token partitions (8.5 MB of partials)
-    c1 = to_device(workloads.paged_case(layers=1, batch=4, n_q_heads=64, n_kv_heads=8,
-                                        head_dim=128, page_size=16,
-                                        ctx=[32768, 1, 20000, 777], dtype="bf16",
-                                        seed=901), "cuda")
+    kw1 = dict(layers=1, batch=4, n_q_heads=64, n_kv_heads=8, head_dim=128, page_size=16,
+               ctx=[32768, 1, 20000, 777], dtype="bf16", seed=901)
     # call 2: different shapes and a plan of its own (automatic partitions)
-    c2 = to_device(workloads.paged_case(layers=1, batch=6, n_q_heads=16, n_kv_heads=4,
-                                        head_dim=64, page_size=16,
-                                        ctx=[3000, 0, 4096, 17, 999, 2500], dtype="fp16",
-                                        seed=902, q_mul=2.0), "cuda")
+    kw2 = dict(layers=1, batch=6, n_q_heads=16, n_kv_heads=4, head_dim=64, page_size=16,
+               ctx=[3000, 0, 4096, 17, 999, 2500], dtype="fp16", seed=902, q_mul=2.0)
+    c1 = to_device(workloads.paged_case(**kw1), "cuda")
+    c2 = to_device(workloads.paged_case(**kw2), "cuda")
+    # both plans split, so both calls go through the shared array
     assert L.pa_decode_workspace_size(4, 64, 8, 128, 16, c1.block_table.shape[2], 512) > 0
+    assert L.pa_decode_workspace_size(6, 16, 4, 64, 16, c2.block_table.shape[2], 0) > 0
     r1 = _reference(L, c1, 512)
     r2 = _reference(L, c2, 0)
     s1 = _static(L, c1, 512)
     s2 = _static(L, c2, 0)
     torch.cuda.synchronize()
-    assert_close(s1.cpu().numpy(), r1.cpu().numpy(), "static workspace, call 1")
-    assert_close(s2.cpu().numpy(), r2.cpu().numpy(), "static workspace, call 2")
     assert pa.pa_last_device_error() == 0
+    for n, (kw, s_out, r_out) in enumerate(((kw1, s1, r1), (kw2, s2, r2)), 1):
+        cpu = workloads.paged_case(**kw)  # the same seeded bytes, on the host
+        ref = oracle.decode(cpu.q[0], cpu.k_cache, cpu.v_cache, cpu.block_table[0],
+                            cpu.ctx_lens, cpu.scale, cpu.dtype_code)
+        assert_close(s_out.cpu().numpy(), ref, f"static workspace, call {n}, vs the oracle")
+        assert_close(s_out.cpu().numpy(), r_out.cpu().numpy(),
+                     f"static workspace, call {n}, vs pa_decode")
 
 
 def test_static_workspace_rejects_plans_beyond_its_array(L):

@@ -180,10 +180,14 @@ int sm_count() {
 // partition count.  Automatic mode, with R = resident CTAs (2 per SM) and
 // I = batch * kv heads * head tiles (CTAs of a single pass):
 //   I <  3R/4: cut sequences into about R / I equal partitions, so that one
-//              wave of CTAs keeps enough copies in flight, of 2 to 256 pages
-//              each (a small call -- a few MB of KV -- is latency-bound: its
-//              short partitions, owned by single warps below, put every page
-//              in flight at once, so the call takes one HBM round trip);
+//              wave of CTAs keeps enough copies in flight, of 16 to 256 pages
+//              each; on the CUDA-core path (group tile 1: MHA), whose per-page
+//              arithmetic is the slow part of a small call, about R / I CTA
+//              slots of single-warp partitions of 2 pages or more instead
+//              (a 4 MB call then holds all its pages in flight at once:
+//              16 heads x 512 tokens, kernel 7.6 -> 6.2 us; 1 x 32 heads x 4k
+//              and 2 x 32 x 2k tokens 25-28% faster; GQA calls were slower
+//              with the bigger merge);
 //   I <  R   : a single pass (one wave, no merge);
 //   I >= R   : cut into 4 partitions of >= 32 pages, so that one long
 //              sequence of a ragged batch cannot make a tail of its own.
@@ -200,11 +204,13 @@ int decode_plan(int batch, int n_q_heads, int n_kv_heads, int max_blocks,
     if (items * 4 < resident * 3) {
       const int64_t want = resident / items > 1 ? resident / items : 1;
       int64_t per = (max_blocks + want - 1) / want;
-      if (per <= 32) {
+      if (group_tile(n_q_heads / n_kv_heads) == 1 && per <= 32) {
         // short partitions go to single warps (below): about `want` CTA
         // slots per item is kDecodeWarps partitions per slot
         per = (max_blocks + want * kDecodeWarps - 1) / (want * kDecodeWarps);
         if (per < 2) per = 2;
+      } else if (per < 16) {
+        per = 16;
       }
       if (per > 256) per = 256;  // longer ranges leave a slow tail (measured at 32k)
       pp = static_cast<int>(per);

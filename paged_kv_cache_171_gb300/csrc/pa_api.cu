@@ -498,6 +498,8 @@ int pa_prefill_paged(const void *q, const void *k_cache, const void *v_cache,
                         max_blocks_per_seq, num_pages, dtype);
   if (rc) return rc;
   if (n_new < 0 || n_new > (1 << 20)) return PA_ERR_SHAPE;
+  if (static_cast<int64_t>(n_new) > static_cast<int64_t>(max_blocks_per_seq) * page_size)
+    return PA_ERR_SHAPE;  // the chunk alone would overflow the table
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_ALIGN;
   if (n_new == 0) return PA_OK;
@@ -529,6 +531,8 @@ int pa_prefill_partition_tokens(int batch, int n_new, int n_q_heads, int n_kv_he
                         max_blocks_per_seq, 1, PA_BF16);
   if (rc) return rc;
   if (n_new < 0 || n_new > (1 << 20)) return PA_ERR_SHAPE;
+  if (static_cast<int64_t>(n_new) > static_cast<int64_t>(max_blocks_per_seq) * page_size)
+    return PA_ERR_SHAPE;  // the chunk alone would overflow the table
   int pt = 0, np = 1;
   rc = prefill_plan(batch, n_new, n_q_heads, n_kv_heads, max_blocks_per_seq,
                     partition_tokens, &pt, &np);
@@ -563,6 +567,8 @@ int pa_prefill_paged_split(const void *q, const void *k_cache, const void *v_cac
                         max_blocks_per_seq, num_pages, dtype);
   if (rc) return rc;
   if (n_new < 0 || n_new > (1 << 20)) return PA_ERR_SHAPE;
+  if (static_cast<int64_t>(n_new) > static_cast<int64_t>(max_blocks_per_seq) * page_size)
+    return PA_ERR_SHAPE;  // the chunk alone would overflow the table
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_ALIGN;
   int pt = 0, np = 1;

@@ -231,3 +231,17 @@ def test_topm_arguments(L):
     assert r(P, 2, 2, 8, 0, 5, P, None, P, 16, None) == -7     # workspace too small
     assert r(P + 4, 2, 2, 8, 0, 5, P, None, P, 1 << 20, None) == -8
     assert r(P, 1 << 16, 1 << 16, 2, 0, 5, P, None, P, 1 << 40, None) == -5
+
+
+def test_chunks_longer_than_the_table_are_rejected(L):
+    """n_new new tokens need n_new slots in the table even with no cache: a
+    longer chunk is refused on the host (the kernels would otherwise clamp
+    the context and still walk past the table row)."""
+    P = FAKE
+    f = ctypes.c_float(0.1)
+    # max_blocks 1 = 16 slots: 17 new tokens cannot fit, 16 can
+    assert L.pa_prefill_paged(P, P, P, P, P, 17, P, f, 8, 8, 128, 16, 2, 1, 16, 0, None) == -5
+    assert L.pa_prefill_paged_split(P, P, P, P, P, 17, P, f, 8, 8, 128, 16, 2, 1, 16, 0, 0,
+                                    None, 0, None) == -5
+    assert L.pa_prefill_partition_tokens(2, 17, 8, 8, 128, 16, 1, 0) == -5
+    assert L.pa_prefill_partition_tokens(2, 16, 8, 8, 128, 16, 1, 0) == 0

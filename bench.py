@@ -541,11 +541,12 @@ def run_window(torch, pa, workloads, steps, warmup, peaks, sink=4, window=4096):
 def run_prefix_sharing(torch, pa, steps, warmup, peaks, B=32, prefix=8192, suffix=128):
     """Prefix sharing through the page pool: B sequences forked from one
     prefix of `prefix` tokens, each with `suffix` tokens of its own (32/8
-    heads, D 128, bf16).  Decode reads the shared pages once per sequence
-    from the block tables; they stay in L2, so logical bytes (as if every
-    sequence held its own copy) move faster than HBM.  The same lengths on
-    unshared pages are timed beside it, and the copy-on-write page copy
-    (pa_copy_pages) on 4096 pages."""
+    heads, D 128, bf16).  pa_decode reads the shared pages once per sequence
+    from the block tables (they stay in L2, so logical bytes -- as if every
+    sequence held its own copy -- move faster than HBM); pa_decode_cascade
+    reads them once for all sequences.  The same lengths on unshared pages are
+    timed beside them, and the copy-on-write page copy (pa_copy_pages) on
+    4096 pages."""
     import numpy as np
     dev = torch.device("cuda", torch.cuda.current_device())
     hq, hkv, D = 32, 8, 128
@@ -602,6 +603,24 @@ def run_prefix_sharing(torch, pa, steps, warmup, peaks, B=32, prefix=8192, suffi
     unique = (n_pref + B * n_own) * hkv * 16 * D * 2 * 2 + B * hq * D * 6
     res["shared"]["unique_bytes"] = unique
     res["shared"]["unique_GB_s"] = round(unique / (res["shared"]["ms_per_step"] * 1e-3) / 1e9, 1)
+    # cascade: the forks' queries over the prefix once, then each fork's own
+    # tokens, merged (pa_decode_cascade)
+    ptab = torch.from_numpy(np.ascontiguousarray(shared[0][:n_pref])).to(dev)
+    own_tab = torch.from_numpy(np.stack([t[n_pref:] for t in shared])).to(dev)
+    own_ctx = torch.full((B,), suffix, dtype=torch.int32, device=dev)
+    cws_bytes = pa.pa_decode_cascade_workspace_size(B, hq, hkv, D, 16, n_pref, prefix, 0)
+    cws = torch.empty(max(1, cws_bytes // 4), dtype=torch.float32, device=dev)
+    ms = time_it(lambda: pa.pa_decode_cascade(q, kc, vc, ptab, prefix, n_pref, own_tab, own_ctx,
+                                              out, 1.0 / D ** 0.5, hq, hkv, D, 16, B, n_own,
+                                              n_pages, pa.BF16, 0, cws, cws_bytes,
+                                              stream.cuda_stream))
+    res["cascade"] = {"ms_per_step": round(ms, 4),
+                      "unique_GB_s": round(unique / (ms * 1e-3) / 1e9, 1),
+                      "frac_of_hbm_peak": round(unique / (ms * 1e-3) / 1e9 /
+                                                peaks.get("hbm_gbs", 6800.0), 4),
+                      "speedup_vs_shared_decode": round(res["shared"]["ms_per_step"] / ms, 3),
+                      "kernels": "prefill_tc_kernel over the prefix (shared keys, key ranges) + "
+                                 "decode_kernel over each fork's own pages + merge_kernel"}
     res["logical_bytes_per_step"] = logical
     res["speedup_vs_unshared"] = round(res["unshared"]["ms_per_step"] /
                                        res["shared"]["ms_per_step"], 3)

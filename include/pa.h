@@ -371,6 +371,46 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
                    size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_cascade -- decode of `batch` forks of one shared prefix, reading
+ * the prefix's K/V once for all of them.
+ *
+ * Prefix sharing (ch. 19 "推理系统与性能工程", 19.7.3: the block tables of
+ * several requests point to the same physical pages): fork b attends the
+ * prefix_len tokens of the shared prefix (pages prefix_table[0 ..
+ * prefix_blocks - 1], device) followed by its own ctx_lens[b] tokens (pages
+ * block_table[b][..], its own table starting at its first own token).  The
+ * result is pa_decode's over the concatenated sequence.  Instead of every
+ * fork streaming the prefix again, the forks' queries are attended to the
+ * prefix together -- one sequence of `batch` queries that all see every
+ * prefix key, on the tensor-core prefill kernel, cut into key ranges -- each
+ * fork's own tokens by the decode kernel, and the partial states (O, m, l) of
+ * both merged exactly (the exponent law of 19.6.2).
+ *   q, out            [batch][n_q_heads][head_dim] (q dtype, out float)
+ *   prefix_len        1 .. prefix_blocks * page_size
+ *   block_table       [batch][max_blocks_per_seq]; ctx_lens[b] >= 0 (0: the
+ *                     fork has no tokens of its own yet)
+ *   partition_tokens  0 = choose, else a multiple of 128: the prefix's key
+ *                     ranges
+ *   workspace         device, pa_decode_cascade_workspace_size(...) bytes,
+ *                     16-byte aligned, owned by the caller; contents on
+ *                     entry do not matter
+ * Returns PA_ERR_SHAPE for a prefix_len outside that range, PA_ERR_WORKSPACE
+ * for a missing or short workspace; otherwise as pa_decode.  Asynchronous on
+ * `stream` (three launches).
+ */
+int pa_decode_cascade(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *prefix_table, int prefix_len, int prefix_blocks,
+                      const int32_t *block_table, const int32_t *ctx_lens, float *out,
+                      float scale, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                      int batch, int max_blocks_per_seq, int num_pages, pa_dtype dtype,
+                      int partition_tokens, void *workspace, size_t workspace_bytes,
+                      pa_stream_t stream);
+/* The workspace pa_decode_cascade needs for these shapes (0 if invalid). */
+size_t pa_decode_cascade_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                        int page_size, int prefix_blocks, int prefix_len,
+                                        int partition_tokens);
+
+/*
  * pa_decode_static_workspace -- pa_decode for callers that cannot allocate.
  *
  * The pages have no counterpart to this entry point: it is a convenience of

@@ -27,7 +27,8 @@ __all__ = [
     "pa_pool_alloc", "pa_pool_share", "pa_pool_release", "pa_pool_prepare_append",
     "pa_copy_pages", "pa_topm_retain", "pa_topm_workspace_size", "topm_retain",
     "pa_last_device_error", "pa_selftest_wait_timeout", "pa_strerror", "decode", "prefill",
-    "prefill_split",
+    "prefill_split", "pa_decode_cascade", "pa_decode_cascade_workspace_size",
+    "decode_cascade",
     "append_kv",
 ]
 
@@ -100,6 +101,10 @@ def lib():
         L.pa_topm_workspace_size.restype = Z
         L.pa_topm_retain.argtypes = [P, I, I, I, I, ctypes.c_longlong, P, P, P, Z, P]
         L.pa_topm_retain.restype = I
+        L.pa_decode_cascade.argtypes = [P, P, P, P, I, I, P, P, P, F] + [I] * 9 + [P, Z, P]
+        L.pa_decode_cascade.restype = I
+        L.pa_decode_cascade_workspace_size.argtypes = [I] * 8
+        L.pa_decode_cascade_workspace_size.restype = Z
         L.pa_decode_static_workspace.argtypes = [P, P, P, P, P, P, F] + [I] * 9 + [P]
         L.pa_decode_static_workspace.restype = I
         L.pa_last_device_error.argtypes = [P]
@@ -247,6 +252,25 @@ def pa_prefill_workspace_size(batch, n_new, n_q_heads, n_kv_heads, head_dim, pag
                               max_blocks_per_seq, partition_tokens=0) -> int:
     return lib().pa_prefill_workspace_size(batch, n_new, n_q_heads, n_kv_heads, head_dim,
                                            page_size, max_blocks_per_seq, partition_tokens)
+
+
+def pa_decode_cascade(q, k_cache, v_cache, prefix_table, prefix_len, prefix_blocks,
+                      block_table, ctx_lens, out, scale, n_q_heads, n_kv_heads, head_dim,
+                      page_size, batch, max_blocks_per_seq, num_pages, dtype, partition_tokens,
+                      workspace, workspace_bytes, stream=None):
+    rc = lib().pa_decode_cascade(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(prefix_table), prefix_len, prefix_blocks,
+        _ptr(block_table), _ptr(ctx_lens), _ptr(out), float(scale), n_q_heads, n_kv_heads,
+        head_dim, page_size, batch, max_blocks_per_seq, num_pages, dtype, partition_tokens,
+        _ptr(workspace), workspace_bytes, _stream(stream))
+    return _check(rc, "pa_decode_cascade")
+
+
+def pa_decode_cascade_workspace_size(batch, n_q_heads, n_kv_heads, head_dim, page_size,
+                                     prefix_blocks, prefix_len, partition_tokens=0) -> int:
+    return lib().pa_decode_cascade_workspace_size(batch, n_q_heads, n_kv_heads, head_dim,
+                                                  page_size, prefix_blocks, prefix_len,
+                                                  partition_tokens)
 
 
 def pa_decode_window(q, k_cache, v_cache, block_table, ctx_lens, out, scale, n_q_heads,
@@ -424,6 +448,29 @@ def prefill_split(q, k_cache, v_cache, block_table, ctx_lens, scale, partition_t
     pa_prefill_paged_split(q, k_cache, v_cache, block_table, ctx_lens, n_new, out, scale,
                            hq, hkv, D, P, B, mb, pages, dtype_code(q), partition_tokens,
                            workspace, ws_bytes, stream)
+    return out
+
+
+def decode_cascade(q, k_cache, v_cache, prefix_table, prefix_len, block_table, ctx_lens,
+                   scale, partition_tokens=0, out=None, workspace=None, stream=None):
+    """pa_decode_cascade on tensors: q [B, h_q, D], one query per fork of a
+    shared prefix of prefix_len tokens (pages prefix_table, int32 [n]);
+    block_table [B, max_blocks] and ctx_lens [B] hold each fork's own tokens
+    after the prefix.  Returns fp32 [B, h_q, D]."""
+    import torch
+    B, hq, D = q.shape
+    pages, hkv, P, _ = k_cache.shape
+    mb = block_table.shape[1]
+    n_pref = prefix_table.shape[0]
+    if out is None:
+        out = torch.empty((B, hq, D), dtype=torch.float32, device=q.device)
+    ws_bytes = pa_decode_cascade_workspace_size(B, hq, hkv, D, P, n_pref, prefix_len,
+                                                partition_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device=q.device)
+    pa_decode_cascade(q, k_cache, v_cache, prefix_table, prefix_len, n_pref, block_table,
+                      ctx_lens, out, scale, hq, hkv, D, P, B, mb, pages, dtype_code(q),
+                      partition_tokens, workspace, ws_bytes, stream)
     return out
 
 

@@ -285,6 +285,38 @@ int prefill_plan(int batch, int n_new, int n_q_heads, int n_kv_heads, int max_bl
   return PA_OK;
 }
 
+// Plan of a cascade decode: the shared prefix's key ranges, cut as
+// pa_prefill_paged_split would cut one sequence whose n_new queries are the
+// forks, but counting only the ranges that hold prefix keys.  Returns the
+// range size in tokens (0: one range) and their number.
+int cascade_plan(int batch, int n_q_heads, int n_kv_heads, int prefix_blocks, int prefix_len,
+                 int partition_tokens, int *part_tokens, int *n_ranges) {
+  int pt = 0, np = 1;
+  const int rc = prefill_plan(1, batch, n_q_heads, n_kv_heads, prefix_blocks, partition_tokens,
+                              &pt, &np);
+  if (rc) return rc;
+  *part_tokens = pt;
+  *n_ranges = pt ? (prefix_len + pt - 1) / pt : 1;
+  return PA_OK;
+}
+
+int check_cascade(int batch, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                  int max_blocks, int num_pages, int dtype, int prefix_blocks, int prefix_len) {
+  const int rc = check_common(n_q_heads, n_kv_heads, head_dim, page_size, batch, max_blocks,
+                              num_pages, dtype);
+  if (rc) return rc;
+  if (batch > (1 << 20) || prefix_blocks <= 0 || prefix_len < 1 ||
+      static_cast<int64_t>(prefix_len) > static_cast<int64_t>(prefix_blocks) * page_size ||
+      static_cast<int64_t>(prefix_blocks) * page_size > (int64_t(1) << 30))
+    return PA_ERR_SHAPE;
+  return PA_OK;
+}
+
+size_t cascade_workspace_bytes(int batch, int n_q_heads, int head_dim, int n_ranges) {
+  return static_cast<size_t>(batch) * n_q_heads * (n_ranges + 1) * (head_dim + 4) *
+         sizeof(float);
+}
+
 }  // namespace
 }  // namespace pa
 
@@ -603,6 +635,106 @@ int pa_prefill_paged_split(const void *q, const void *k_cache, const void *v_cac
   a.part_tokens = pt;
   a.workspace = np > 1 ? static_cast<float *>(workspace) : nullptr;
   return launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t pa_decode_cascade_workspace_size(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                        int page_size, int prefix_blocks, int prefix_len,
+                                        int partition_tokens) {
+  if (check_cascade(batch, n_q_heads, n_kv_heads, head_dim, page_size, 1, 1, PA_BF16,
+                    prefix_blocks, prefix_len))
+    return 0;
+  int pt = 0, nr = 1;
+  if (cascade_plan(batch, n_q_heads, n_kv_heads, prefix_blocks, prefix_len, partition_tokens,
+                   &pt, &nr))
+    return 0;
+  return cascade_workspace_bytes(batch, n_q_heads, head_dim, nr);
+}
+
+int pa_decode_cascade(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *prefix_table, int prefix_len, int prefix_blocks,
+                      const int32_t *block_table, const int32_t *ctx_lens, float *out,
+                      float scale, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                      int batch, int max_blocks_per_seq, int num_pages, pa_dtype dtype,
+                      int partition_tokens, void *workspace, size_t workspace_bytes,
+                      pa_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !prefix_table || !block_table || !ctx_lens || !out ||
+      !workspace)
+    return PA_ERR_NULL;
+  int rc = check_cascade(batch, n_q_heads, n_kv_heads, head_dim, page_size,
+                         max_blocks_per_seq, num_pages, dtype, prefix_blocks, prefix_len);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(workspace))
+    return PA_ERR_ALIGN;
+  int pt = 0, nr = 1;
+  rc = cascade_plan(batch, n_q_heads, n_kv_heads, prefix_blocks, prefix_len, partition_tokens,
+                    &pt, &nr);
+  if (rc) return rc;
+  if (workspace_bytes < cascade_workspace_bytes(batch, n_q_heads, head_dim, nr))
+    return PA_ERR_WORKSPACE;
+  int *status = nullptr;
+  rc = current_status_ptr(&status);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float *ws = static_cast<float *>(workspace);
+  // 1. every fork's queries over the shared prefix at once: one sequence
+  //    whose n_new = batch queries all see keys 0 .. prefix_len - 1; partial
+  //    states in slots 0 .. nr - 1 of each (fork, head) row
+  PrefillLaunch a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = prefix_table;
+  a.ctx_lens = ctx_lens;  // not read with shared keys
+  a.out = out;            // not written while partial states go to the workspace
+  a.status = status;
+  a.scale = scale;
+  a.n_new = batch;
+  a.n_q_heads = n_q_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.head_dim = head_dim;
+  a.batch = 1;
+  a.max_blocks = prefix_blocks;
+  a.num_pages = num_pages;
+  a.bf16 = dtype == PA_BF16;
+  a.n_parts = nr;
+  a.part_tokens = pt;
+  a.workspace = ws;
+  a.shared_ctx = prefix_len;
+  a.ws_slots = nr + 1;
+  a.merge = false;
+  rc = launch_prefill(a, s);
+  if (rc) return rc;
+  // 2. each fork's own tokens: a single-pass decode whose state goes to slot
+  //    nr (a separate merge folds all rows in parallel: folding the prefix's
+  //    states in the decode's epilogue, one element after another, was slower)
+  DecodeLaunch d;
+  d.q = q;
+  d.k_cache = k_cache;
+  d.v_cache = v_cache;
+  d.block_table = block_table;
+  d.ctx_lens = ctx_lens;
+  d.out = out;
+  d.workspace = nullptr;
+  d.status = status;
+  d.scale = scale;
+  d.n_q_heads = n_q_heads;
+  d.n_kv_heads = n_kv_heads;
+  d.head_dim = head_dim;
+  d.batch = batch;
+  d.max_blocks = max_blocks_per_seq;
+  d.num_pages = num_pages;
+  d.bf16 = dtype == PA_BF16;
+  d.part_pages = 0;
+  d.n_parts = 1;
+  d.warp_parts = 0;
+  d.part = ws;
+  d.part_stride = nr + 1;
+  d.part_slot = nr;
+  rc = launch_decode(d, s);
+  if (rc) return rc;
+  // 3. the exponent law over the nr + 1 states of every row (19.6.2)
+  return launch_merge_all(ws, out, status, batch, n_q_heads, head_dim, nr + 1, s);
 }
 
 int pa_last_device_error(pa_stream_t stream) {

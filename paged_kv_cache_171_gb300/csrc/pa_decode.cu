@@ -67,6 +67,12 @@ struct DecodeParams {
   int warp_parts;  // > 0: each warp owns this many whole partitions
   int sink, window;  // window >= 0: only the first `sink` and the last
                      // `window` keys of each sequence are attended
+  // Single pass only: with part set, each row's state (O unnormalised,
+  // m in natural-log units, l) goes to slot part_slot of part
+  // [row][part_stride][D + 4] instead of O / l to out (the own keys of a
+  // cascade decode, merged with the shared prefix's states afterwards).
+  float *part;
+  int part_stride, part_slot;
 };
 
 // The keys a sequence's query attends, as a list of virtual pages.  Without
@@ -530,10 +536,19 @@ __global__ void __launch_bounds__(NW * 32)
   }
   const int n_active = cta_pages > 0 ? (n_pages + cta_pages - 1) / cta_pages : 1;
   if (pg0 >= pg1) {
-    // Nothing to read.  An empty sequence owes zeros (CTA 0 writes them).
-    if (blockIdx.x == 0)
-      for (int i = tid; i < GT * D; i += NW * 32)
-        p.out[(static_cast<size_t>(b) * p.n_q_heads + h0) * D + i] = 0.f;
+    // Nothing to read.  An empty sequence owes zeros (CTA 0 writes them), or
+    // an empty state (O = 0, m = -inf, l = 0).
+    if (blockIdx.x == 0) {
+      for (int i = tid; i < GT * (D + 4); i += NW * 32) {
+        const size_t row = static_cast<size_t>(b) * p.n_q_heads + h0 + i / (D + 4);
+        const int d = i % (D + 4);
+        if (!p.part) {
+          if (d < D) p.out[row * D + d] = 0.f;
+        } else if (d < D + 2) {
+          p.part[(row * p.part_stride + p.part_slot) * (D + 4) + d] = d == D ? -INFINITY : 0.f;
+        }
+      }
+    }
     return;
   }
 
@@ -717,7 +732,16 @@ __global__ void __launch_bounds__(NW * 32)
     }
     const size_t row = row0 + h;
     if constexpr (!SPLIT) {
-      p.out[row * D + d] = lt > 0.f ? o / lt : 0.f;
+      if (!p.part) {
+        p.out[row * D + d] = lt > 0.f ? o / lt : 0.f;
+      } else {
+        float *dst = p.part + (row * p.part_stride + p.part_slot) * (D + 4);
+        dst[d] = o;
+        if (d == 0) {
+          dst[D] = M * kLn2;  // natural-log units
+          dst[D + 1] = lt;
+        }
+      }
     } else {
       float *dst = p.ws + (row * p.n_parts + blockIdx.x) * (D + 4);
       dst[d] = o;
@@ -816,7 +840,9 @@ __global__ void clear_counters_kernel(int *ctr, int n) {
 // threads per row.  A row is (sequence b, query i < q_len, head h), stored at
 // (b q_len + i) n_q_heads + h; it saw T = ctx[b] keys (decode), or
 // ctx[b] + i + 1 (prefill: query i of a chunk that follows ctx[b] cached
-// tokens), so its partitions 0 .. ceil(T / part_tokens) - 1 hold states.  Thread (sl, qd) owns a float4 of head_dim
+// tokens), so its partitions 0 .. ceil(T / part_tokens) - 1 hold states; or
+// (mode 2, a cascade decode) every one of its n_parts slots holds a state,
+// possibly empty (l = 0).  Thread (sl, qd) owns a float4 of head_dim
 // and every SL-th partition, and folds its partitions into a running
 // (m, l, O) with the same law as it reads them, so all its loads are
 // independent and a row costs about one memory round trip; the SL slices
@@ -833,16 +859,19 @@ __global__ void __launch_bounds__(128)
   const int q_len = gridDim.x / n_q_heads, tid = threadIdx.x;
   griddep_release();
   griddep_wait();
-  long T = ctx[b];
-  if (T < 0) {
-    if (tid == 0 && blockIdx.x == 0) record_error(status, PA_ERR_BAD_CTX);
-    T = 0;
-  }
-  if (prefill) T += i + 1;
-  int n_valid = static_cast<int>((T + part_tokens - 1) / part_tokens);
-  if (n_valid > n_parts) {
-    if (tid == 0 && blockIdx.x == 0) record_error(status, PA_ERR_BAD_CTX);
-    n_valid = n_parts;
+  int n_valid = n_parts;
+  if (prefill != 2) {
+    long T = ctx[b];
+    if (T < 0) {
+      if (tid == 0 && blockIdx.x == 0) record_error(status, PA_ERR_BAD_CTX);
+      T = 0;
+    }
+    if (prefill) T += i + 1;
+    n_valid = static_cast<int>((T + part_tokens - 1) / part_tokens);
+    if (n_valid > n_parts) {
+      if (tid == 0 && blockIdx.x == 0) record_error(status, PA_ERR_BAD_CTX);
+      n_valid = n_parts;
+    }
   }
   const size_t row = (static_cast<size_t>(b) * q_len + i) * n_q_heads + h;
   const float *base = parts + row * static_cast<size_t>(n_parts) * W;
@@ -934,6 +963,9 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   p.warp_parts = a.warp_parts;
   p.sink = a.sink;
   p.window = a.window;
+  p.part = a.part;
+  p.part_stride = a.part_stride;
+  p.part_slot = a.part_slot;
   const dim3 grid(gx, a.n_kv_heads * (p.group / GT), a.batch);
   if (split) {
     p.ctr = reinterpret_cast<int *>(reinterpret_cast<char *>(a.workspace) +
@@ -984,6 +1016,18 @@ int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,
     merge_kernel<64><<<grid, 128, 0, stream>>>(partials, ctx_lens, out, status,
                                                n_q_heads, n_parts, partition_tokens, 0);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int launch_merge_all(const float *partials, float *out, int *status, int n_rows, int n_q_heads,
+                     int head_dim, int n_slots, cudaStream_t stream) {
+  const dim3 grid(n_q_heads * n_rows, 1);
+  const cudaError_t e =
+      head_dim == 128
+          ? launch_pdl(merge_kernel<128>, grid, dim3(128), 0, stream, partials,
+                       static_cast<const int32_t *>(nullptr), out, status, n_q_heads, n_slots, 1, 2)
+          : launch_pdl(merge_kernel<64>, grid, dim3(128), 0, stream, partials,
+                       static_cast<const int32_t *>(nullptr), out, status, n_q_heads, n_slots, 1, 2);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int launch_merge_rows(const float *partials, const int32_t *ctx_lens, float *out, int *status,

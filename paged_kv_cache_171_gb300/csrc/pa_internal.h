@@ -87,6 +87,11 @@ struct DecodeLaunch {
   // and t >= T - window (window < 0: every key).  Partitions then cut the
   // attended keys' pages.
   int sink = 0, window = -1;
+  // Single pass only (part_pages 0): each row's partial state goes to slot
+  // part_slot of part [row][part_stride][head_dim + 4] instead of O / l to
+  // out (the own keys of a cascade decode).
+  float *part = nullptr;
+  int part_stride = 0, part_slot = 0;
 };
 
 constexpr int kDecodeWarps = 4;  // warps per decode CTA
@@ -119,6 +124,12 @@ int launch_merge(const float *partials, const int32_t *ctx_lens, float *out,
                  int *status, int batch, int n_q_heads, int head_dim,
                  int n_parts, int partition_tokens, cudaStream_t stream);
 
+// Merge of every slot of each row: rows n_rows x n_q_heads, partials
+// [row][n_slots][head_dim + 4] (empty slots carry l = 0).
+int launch_merge_all(const float *partials, float *out, int *status, int n_rows, int n_q_heads,
+                     int head_dim, int n_slots, cudaStream_t stream);
+
+
 int launch_append(const void *k_new, const void *v_new, void *k_cache,
                   void *v_cache, const int32_t *block_table,
                   const int32_t *seq_idx, const int32_t *pos, int *status,
@@ -140,6 +151,12 @@ struct PrefillLaunch {
   // 128); partial states go to workspace, then a merge writes out.
   int n_parts = 1, part_tokens = 0;
   float *workspace = nullptr;
+  // Shared keys (cascade decode): shared_ctx >= 0 makes every query attend
+  // keys 0 .. shared_ctx - 1 of its sequence's table, no causal mask; with a
+  // workspace, ws_slots (0: n_parts) partial-state slots per row, and merge =
+  // false leaves the partial states for the caller to fold.
+  int shared_ctx = -1, ws_slots = 0;
+  bool merge = true;
 };
 
 // Workspace of a split prefill: float [B][n_new][Hq][n_parts][D + 4].

@@ -107,11 +107,15 @@ struct TcParams {
   uint32_t qsign;   // 0x80008000 when scale < 0 (folded into Q), else 0
   int n_new, n_q_heads, n_kv_heads, group, batch, max_blocks, num_pages;
   // Key-range partitions: n_parts > 1 splits each sequence's keys into
-  // ranges of part_tiles key tiles; every CTA then writes its rows' partial
-  // states (O, m, l) to ws [batch][n_new][n_q_heads][n_parts][head_dim + 4]
-  // for the merge kernel instead of O / l to out.
+  // ranges of part_tiles key tiles.  With ws set, every CTA writes its rows'
+  // partial states (O, m, l) to ws [batch][n_new][n_q_heads][ws_slots]
+  // [head_dim + 4] (slot = its range) for a merge instead of O / l to out.
   float *ws;
-  int part_tiles, n_parts;
+  int part_tiles, n_parts, ws_slots;
+  // shared_ctx >= 0: every query of a sequence attends the same keys
+  // 0 .. shared_ctx - 1 (ctx_lens unused, no causal mask): the forks of a
+  // shared prefix, queried once for all of them.
+  int shared_ctx;
 };
 
 // Shared memory (offsets from a 1024-aligned base).  Operand tiles are
@@ -465,9 +469,10 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
   const int qi = rr / GT, hh = rr % GT;
   const bool rem = SR && r >= 64;  // this warp writes the remainder terms
   const int qx0 = w.qx[x];
-  const int kmax_x = w.ctx + qx0 + w.nq[x] - 1;
-  const int lim = min(w.ctx + qx0 + qi, kmax_x);  // last key row r sees
-  const int lim_all = w.ctx + qx0;                // every row of x sees keys <= this
+  const bool shared = p.shared_ctx >= 0;  // every row sees keys < ctx
+  const int kmax_x = shared ? w.ctx - 1 : w.ctx + qx0 + w.nq[x] - 1;
+  const int lim = shared ? kmax_x : min(w.ctx + qx0 + qi, kmax_x);  // last key row r sees
+  const int lim_all = shared ? kmax_x : w.ctx + qx0;  // every row of x sees keys <= this
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tSx = tmem + x * kKeys + lane_base;      // S_x, then P_x
   const uint32_t tOx = tmem + 2 * kKeys + x * D + lane_base;
@@ -677,11 +682,11 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
   tc::fence_after_sync();
 
   // ---- O / l for this row, or the row's partial state for this key range
-  const bool split = p.n_parts > 1;
+  const bool split = p.ws != nullptr;
   const float inv = split ? 1.f : (l > 0.f ? 1.f / l : 0.f);
   const size_t row =
       (static_cast<size_t>(w.b) * p.n_new + qx0 + qi) * p.n_q_heads + w.hbase + hh;
-  float *dst = split ? p.ws + (row * p.n_parts + w.part) * (D + 4) : p.out + row * D;
+  float *dst = split ? p.ws + (row * p.ws_slots + w.part) * (D + 4) : p.out + row * D;
   // columns 32 c .. 32 c + 31 of this lane's O (interleaved: both tiles' merged)
   auto load_o = [&](int c, uint32_t (&o)[32]) {
     tc::ld32(tOx + c * 32, o);
@@ -766,17 +771,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   w.part = blockIdx.x % p.n_parts;
   w.q0 = (blockIdx.x / p.n_parts) * 2 * BQ;
   w.t0 = w.part * p.part_tiles;  // part_tiles = every tile when n_parts is 1
-  int ctx = p.ctx_lens[w.b];
+  const bool shared = p.shared_ctx >= 0;
   const int maxT = p.max_blocks * 16;
-  if (ctx < 0 || ctx + p.n_new > maxT) {
-    if (tid == 0) record_error(p.status, PA_ERR_BAD_CTX);
-    ctx = max(0, min(ctx, maxT - p.n_new));
+  int ctx;
+  if (shared) {
+    ctx = p.shared_ctx;  // checked against the table on the host (at least 1 key)
+  } else {
+    ctx = p.ctx_lens[w.b];
+    if (ctx < 0 || ctx + p.n_new > maxT) {
+      if (tid == 0) record_error(p.status, PA_ERR_BAD_CTX);
+      ctx = max(0, min(ctx, maxT - p.n_new));
+    }
   }
   w.ctx = ctx;
   w.kmax = -1;
   for (int x = 0; x < 2; ++x) {
     w.nq[x] = max(0, min(BQ, p.n_new - (w.q0 + x * BQ)));
-    const int kx = ctx + w.q0 + x * BQ + w.nq[x] - 1;  // last key a row of x sees
+    // last key a row of x sees
+    const int kx = shared ? ctx - 1 : ctx + w.q0 + x * BQ + w.nq[x] - 1;
     const int t_end = min(kx / kKeys + 1, w.t0 + p.part_tiles);
     w.n_tiles[x] = w.nq[x] > 0 ? max(0, t_end - w.t0) : 0;
     if (w.nq[x] > 0) w.kmax = max(w.kmax, kx);
@@ -792,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     w.n_tiles[0] -= w.n_tiles[1];
   }
   w.sr = w.il && w.nq[0] * GT <= kRows / 2;
-  const int n_pages = (ctx + p.n_new + 15) >> 4;
+  const int n_pages = (ctx + (shared ? 0 : p.n_new) + 15) >> 4;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kSlot + 4);
   volatile int *mode = reinterpret_cast<volatile int *>(smem + L::kSlot + 8);  // [2]
   volatile int *votes = reinterpret_cast<volatile int *>(smem + L::kVote);     // [2][4]
@@ -909,12 +921,14 @@ int launch_tc_t(const PrefillLaunch &a, cudaStream_t stream) {
   p.ws = a.workspace;
   p.n_parts = a.n_parts > 1 ? a.n_parts : 1;
   p.part_tiles = a.n_parts > 1 ? a.part_tokens / kKeys : (a.max_blocks * 16 + kKeys - 1) / kKeys;
+  p.ws_slots = a.ws_slots > 0 ? a.ws_slots : p.n_parts;
+  p.shared_ctx = a.shared_ctx;
   constexpr int BQ = kRows / GT;
   const dim3 grid(((a.n_new + 2 * BQ - 1) / (2 * BQ)) * p.n_parts,
                   a.n_kv_heads * (p.group / GT), a.batch);
   if (launch_pdl(kern, grid, dim3(kThreads), L::kAlloc, stream, kmap, vmap, p) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (p.n_parts > 1)
+  if (p.n_parts > 1 && a.merge)
     return launch_merge_rows(a.workspace, a.ctx_lens, a.out, a.status, a.batch, a.n_q_heads,
                              D, p.n_parts, a.part_tokens, a.n_new, stream);
   return PA_OK;

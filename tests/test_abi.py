@@ -245,3 +245,28 @@ def test_chunks_longer_than_the_table_are_rejected(L):
                                     None, 0, None) == -5
     assert L.pa_prefill_partition_tokens(2, 17, 8, 8, 128, 16, 1, 0) == -5
     assert L.pa_prefill_partition_tokens(2, 16, 8, 8, 128, 16, 1, 0) == 0
+
+
+def test_cascade_arguments_and_workspace(L):
+    P = FAKE
+    f = ctypes.c_float(0.1)
+    ws = L.pa_decode_cascade_workspace_size(32, 32, 8, 128, 16, 512, 8192, 512)
+    # [batch][n_q_heads][prefix ranges + 1][head_dim + 4] floats: 16 ranges of
+    # 512 and the forks' own keys
+    assert ws == 32 * 32 * (16 + 1) * (128 + 4) * 4
+    assert L.pa_decode_cascade_workspace_size(32, 32, 8, 128, 16, 512, 8192, 100) == 0
+    assert L.pa_decode_cascade_workspace_size(32, 32, 8, 128, 16, 512, 0, 0) == 0
+    assert L.pa_decode_cascade_workspace_size(32, 32, 8, 128, 16, 512, 8193, 0) == 0
+    c = L.pa_decode_cascade
+    # prefix_len outside [1, prefix_blocks * page_size], null, short workspace,
+    # bad partition: all before any launch
+    assert c(P, P, P, P, 0, 512, P, P, P, f, 32, 8, 128, 16, 32, 8, 1024, 0, 0, P, ws,
+             None) == -5
+    assert c(P, P, P, P, 8193, 512, P, P, P, f, 32, 8, 128, 16, 32, 8, 1024, 0, 0, P, ws,
+             None) == -5
+    assert c(P, P, P, None, 8192, 512, P, P, P, f, 32, 8, 128, 16, 32, 8, 1024, 0, 0, P, ws,
+             None) == -1
+    assert c(P, P, P, P, 8192, 512, P, P, P, f, 32, 8, 128, 16, 32, 8, 1024, 0, 512, P,
+             ws - 4, None) == -7
+    assert c(P, P, P, P, 8192, 512, P, P, P, f, 32, 8, 128, 16, 32, 8, 1024, 0, 100, P, ws,
+             None) == -9

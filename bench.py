@@ -938,6 +938,19 @@ def ncu_case(args):
         sc = (torch.randn(32, 32, 32768, generator=g, device="cuda") * 16).round() / 16
         for _ in range(args.warmup + args.steps):
             pa.topm_retain(sc, 32767, 32 * 32 * 32768 // 4)
+    elif args.ncu_case == "cascade":  # 32 forks of an 8192-token prefix + 128 own tokens
+        B, hq, hkv, D, prefix, suffix = 32, 32, 8, 128, 8192, 128
+        n_pref, n_own = prefix // 16, suffix // 16
+        g = torch.Generator(device="cuda").manual_seed(1008)
+        pages = n_pref + B * n_own
+        kc = torch.randn(pages, hkv, 16, D, generator=g, device="cuda").to(torch.bfloat16)
+        vc = torch.randn(pages, hkv, 16, D, generator=g, device="cuda").to(torch.bfloat16)
+        q = torch.randn(B, hq, D, generator=g, device="cuda").to(torch.bfloat16)
+        ptab = torch.arange(n_pref, dtype=torch.int32, device="cuda")
+        own = (n_pref + torch.arange(B * n_own, dtype=torch.int32, device="cuda")).view(B, n_own)
+        own_ctx = torch.full((B,), suffix, dtype=torch.int32, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            pa.decode_cascade(q, kc, vc, ptab, prefix, own, own_ctx, 1.0 / math.sqrt(D))
     elif args.ncu_case == "copy_pages":  # 4096 page pairs, 8 kv heads, D 128, bf16
         kc = torch.zeros(8192, 8, 16, 128, dtype=torch.bfloat16, device="cuda")
         vc = torch.zeros_like(kc)
@@ -970,7 +983,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", choices=["decode", "decode_gqa8", "decode_gqa4",
                                            "decode_mha_small", "verify", "window", "topm",
-                                           "copy_pages", "prefill"],
+                                           "copy_pages", "prefill", "cascade"],
                     help="run a small launch sequence for an ncu capture and exit")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -825,24 +825,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (zeros past the chunk's end; the sign of a negative scale folded in).
   // Interleaved, only Q_A is loaded: Q_B's space belongs to the K ring.
   if (warp >= kSoftmaxWarp0 && !(w.il && warp >= kSoftmaxWarp0 + 4)) {
+    // A thread's loads all go out before its first store (each store is a
+    // compiler barrier), so they cost one memory round trip, not sixteen.
     const int x = (warp - kSoftmaxWarp0) >> 2;
-    for (int e = tid & 127; e < kRows * (D / 8); e += 128) {
-      const int r = e / (D / 8), c = e % (D / 8);
+    constexpr int kPer = kRows * (D / 8) / 128;  // 16-byte chunks per thread
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = (tid & 127) + 128 * k, r = e / (D / 8), c = e % (D / 8);
       const int rr = w.sr ? (r & 63) : r;  // split rows: rows 64-127 repeat 0-63
       const int qi = rr / GT, hh = rr % GT;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (qi < w.nq[x]) {
-        v = *reinterpret_cast<const uint4 *>(
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (qi < w.nq[x])
+        v[k] = __ldg(reinterpret_cast<const uint4 *>(
             p.q +
-            ((static_cast<size_t>(w.b) * p.n_new + w.qx[x] + qi) * p.n_q_heads +
-             w.hbase + hh) * D + c * 8);
-        v.x ^= p.qsign;
-        v.y ^= p.qsign;
-        v.z ^= p.qsign;
-        v.w ^= p.qsign;
-      }
-      st_shared_v4(sb + L::kQ + x * L::kQBytes + (c >> 3) * L::kColBlk + swz128(r, c), v.x,
-                   v.y, v.z, v.w);
+            ((static_cast<size_t>(w.b) * p.n_new + w.qx[x] + qi) * p.n_q_heads + w.hbase +
+             hh) * D + c * 8));
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = (tid & 127) + 128 * k, r = e / (D / 8), c = e % (D / 8);
+      st_shared_v4(sb + L::kQ + x * L::kQBytes + (c >> 3) * L::kColBlk + swz128(r, c),
+                   v[k].x ^ p.qsign, v[k].y ^ p.qsign, v[k].z ^ p.qsign, v[k].w ^ p.qsign);
     }
     fence_proxy_async_smem();  // generic stores -> read by the tensor cores
   }

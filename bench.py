@@ -3,10 +3,11 @@
 
 Headline workload (one "step" = one decode step of a 32-layer model): the
 GQA continuous-batching batch, the largest decode workload that the pages
-describe.  For each of 32 layers, pa_append_kv writes the step's new K/V row
-of every sequence into its page, then pa_decode attends each query head over
-the sequence's cached tokens (paged gather, online softmax, split-K
-partitions and their exact merge).  64 sequences with seeded lengths drawn
+describe.  For each of 32 layers, one pa_decode_append call writes the step's
+new K/V row of every sequence into its page and attends each query head over
+the sequence's cached tokens, the new one included (paged gather, online
+softmax, split-K partitions and their exact merge; pa_append_kv + pa_decode
+in one kernel).  64 sequences with seeded lengths drawn
 uniformly from [128, 8192], 32 query heads sharing 8 KV heads (GQA-4),
 head_dim 128, bf16 KV, page_size 16, random block tables, Q drawn N(0,1) x 2
 (peaky softmax).  The LLaMA-7B-shaped step (batch 8, 32/32 heads, context
@@ -182,8 +183,10 @@ def gpu_uuid(torch):
 # our arm
 
 def run_decode_step(torch, pa, workloads, name, args, rank, world):
-    """The decode step of one 32-layer workload: per layer, pa_append_kv of
-    the step's token, then pa_decode over every cached token."""
+    """The decode step of one 32-layer workload: per layer, the step's token's
+    K/V written into the cache and the decode over every cached token, new
+    one included -- one pa_decode_append call (pa_append_kv + pa_decode in
+    one kernel; the two-call form is timed beside it)."""
     cfg = workloads.CONFIGS[name]
     dev = torch.device("cuda", torch.cuda.current_device())
     case = workloads.config_case(name, device=dev)
@@ -205,20 +208,27 @@ def run_decode_step(torch, pa, workloads, name, args, rank, world):
     dcode = case.dtype_code
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
-    launches_per_layer = 2 + (1 if part else 0)
+    launches_per_layer = 1 + (1 if part else 0)
 
     def step(ev=None):
+        for layer in range(L):
+            if ev is not None:
+                ev[layer][0].record(stream)
+            pa.pa_decode_append(case.q[layer], k_new[layer], v_new[layer], case.k_cache,
+                                case.v_cache, case.block_table[layer], ctx, out[layer],
+                                case.scale, hq, hkv, D, 16, B, mb, pages, dcode, 0, ws,
+                                ws_bytes, sptr)
+            if ev is not None:
+                ev[layer][1].record(stream)
+
+    def step_two_calls():
         for layer in range(L):
             pa.pa_append_kv(k_new[layer], v_new[layer], case.k_cache, case.v_cache,
                             case.block_table[layer], seq_idx, pos, B, hkv, D, 16, B, mb,
                             pages, dcode, sptr)
-            if ev is not None:
-                ev[layer][0].record(stream)
             pa.pa_decode(case.q[layer], case.k_cache, case.v_cache, case.block_table[layer],
                          ctx, out[layer], case.scale, hq, hkv, D, 16, B, mb, pages, dcode,
                          0, ws, ws_bytes, sptr)
-            if ev is not None:
-                ev[layer][1].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -247,7 +257,18 @@ def run_decode_step(torch, pa, workloads, name, args, rank, world):
     ms = t0.elapsed_time(t1)
     ms_max = allreduce_max(torch, world, ms)
 
-    # The dominant call (pa_decode) timed on its own
+    # The same steps as pa_append_kv + pa_decode per layer, for comparison
+    for _ in range(2):
+        step_two_calls()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step_two_calls()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    two_call_ms = t0.elapsed_time(t1)
+
+    # The dominant call (pa_decode_append) timed on its own
     # stream with events around each call, over the same number of steps.
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
           for _ in range(args.steps)]
@@ -263,7 +284,7 @@ def run_decode_step(torch, pa, workloads, name, args, rank, world):
         "q": case.q.cpu().pin_memory(),
         "k_new": k_new.cpu().pin_memory(), "v_new": v_new.cpu().pin_memory(),
         "block_table": case.block_table.cpu().pin_memory(),
-        "ctx_lens": ctx.cpu().pin_memory(), "pos": pos.cpu().pin_memory(),
+        "ctx_lens": ctx.cpu().pin_memory(),
     }
     dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -283,8 +304,7 @@ def run_decode_step(torch, pa, workloads, name, args, rank, world):
     def step_e2e():
         copy_stream.wait_stream(stream)  # the previous step is done with dev_in
         with torch.cuda.stream(copy_stream):
-            for k in ("ctx_lens", "pos"):
-                dev_in[k].copy_(host_in[k], non_blocking=True)
+            dev_in["ctx_lens"].copy_(host_in["ctx_lens"], non_blocking=True)
             for gi, (a, b) in enumerate(groups):
                 for k in per_layer_in:
                     dev_in[k][a:b].copy_(host_in[k][a:b], non_blocking=True)
@@ -292,13 +312,11 @@ def run_decode_step(torch, pa, workloads, name, args, rank, world):
         for gi, (a, b) in enumerate(groups):
             stream.wait_event(ev_in[gi])
             for layer in range(a, b):
-                pa.pa_append_kv(dev_in["k_new"][layer], dev_in["v_new"][layer], case.k_cache,
-                                case.v_cache, dev_in["block_table"][layer], seq_idx,
-                                dev_in["pos"], B, hkv, D, 16, B, mb, pages, dcode, sptr)
-                pa.pa_decode(dev_in["q"][layer], case.k_cache, case.v_cache,
-                             dev_in["block_table"][layer], dev_in["ctx_lens"], out[layer],
-                             case.scale, hq, hkv, D, 16, B, mb, pages, dcode, 0, ws,
-                             ws_bytes, sptr)
+                pa.pa_decode_append(dev_in["q"][layer], dev_in["k_new"][layer],
+                                    dev_in["v_new"][layer], case.k_cache, case.v_cache,
+                                    dev_in["block_table"][layer], dev_in["ctx_lens"],
+                                    out[layer], case.scale, hq, hkv, D, 16, B, mb, pages,
+                                    dcode, 0, ws, ws_bytes, sptr)
             ev_out[gi].record(stream)
         with torch.cuda.stream(copy_stream):
             for gi, (a, b) in enumerate(groups):
@@ -322,6 +340,7 @@ def run_decode_step(torch, pa, workloads, name, args, rank, world):
         name=name, cfg=cfg,
         case=case, ms=ms_max, step_bytes=step_bytes, per_layer_bytes=per_layer_bytes,
         call_avg_ms=call_avg_ms, clocks=clocks, part=part, L=L, B=B,
+        two_call_ms=two_call_ms / args.steps,
         launches=args.steps * L * launches_per_layer,
         e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ctx_list=ctx_list,
     )
@@ -721,7 +740,8 @@ def describe(name, cfg):
     pool = (f"shuffled pool of {cfg['pool_pages']} pages" if cfg.get("pool_pages")
             else "random block tables")
     qm = f", Q x {cfg['q_mul']:g}" if cfg.get("q_mul", 1.0) != 1.0 else ""
-    return (f"{name}: decode step of {cfg['layers']} layers x (pa_append_kv + pa_decode), "
+    return (f"{name}: decode step of {cfg['layers']} layers x pa_decode_append (the step "
+            f"token's K/V write + decode), "
             f"batch {cfg['batch']}, {cfg['n_q_heads']} q heads / {cfg['n_kv_heads']} kv "
             f"heads, head_dim {cfg['head_dim']}, {ctx_s}, {cfg['dtype']} KV, page_size "
             f"{cfg['page_size']}, {pool}{qm}")
@@ -732,7 +752,14 @@ def step_block(r, args, world, peaks, peaks_src):
     ms_step = r["ms"] / args.steps
     value = whole_job_gbs(world, r["step_bytes"], ms_step)
     seq_layers = world * r["L"] * r["B"] / (ms_step * 1e-3)
-    call_gbs = r["per_layer_bytes"] / (r["call_avg_ms"] * 1e-3) / 1e9
+    # The timed region is L decode launches per step, back to back (plus, for
+    # split plans, one 1-CTA counter clear per launch that overlaps it under
+    # programmatic dependent launch): its time over those launches is the
+    # kernel's average launch duration.  Events around each call stop that
+    # overlap, so that figure is reported apart.
+    launch_ms = r["ms"] / (args.steps * r["L"])
+    call_gbs = r["per_layer_bytes"] / (launch_ms * 1e-3) / 1e9
+    isolated_gbs = r["per_layer_bytes"] / (r["call_avg_ms"] * 1e-3) / 1e9
     e2e_ms_step = r["e2e_ms"] / args.steps
     hbm = peaks.get("hbm_gbs", 6800.0)
     tr = traffic_record(r["name"])
@@ -756,16 +783,23 @@ def step_block(r, args, world, peaks, peaks_src):
                      "unit": "GB/s", "frac": round(call_gbs / hbm, 4),
                      "traffic": tr["dram_bytes_per_launch"] if tr else None,
                      "peak_source": f"{peaks_src} hbm_gbs (copy)",
-                     "kernel": "pa_decode call (decode_kernel; split plans merge in the "
-                               "last CTA of each head group)",
+                     "kernel": "pa_decode_append call (decode_kernel with the step's K/V "
+                               "write; split plans merge in the last CTA of each head group)",
                      "algorithmic_bytes_per_launch": r["per_layer_bytes"],
-                     "avg_launch_ms": round(r["call_avg_ms"], 5),
+                     "avg_launch_ms": round(launch_ms, 5),
+                     "avg_launch_ms_from": "timed region / decode launches in it",
+                     "isolated_call_ms": round(r["call_avg_ms"], 5),
+                     "isolated_call_frac": round(isolated_gbs / hbm, 4),
                      "traffic_capture": tr["capture"] if tr else None},
         "e2e": {"value": round(whole_job_gbs(world, r["step_bytes"], e2e_ms_step), 1),
                 "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms_step, 4)},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
+        "append_then_decode": {
+            "ms_per_step": round(r["two_call_ms"], 4),
+            "value": round(whole_job_gbs(world, r["step_bytes"], r["two_call_ms"]), 1),
+            "unit": "GB/s", "calls": "pa_append_kv + pa_decode per layer"},
     }
 
 
@@ -814,6 +848,12 @@ def main_ours(args):
     rank, world = init_dist(torch, args)
     peaks, peaks_src = measured_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
+    if args.only_second:  # the LLaMA-7B-shaped step alone (profiling runs)
+        r2 = run_decode_step(torch, pa, workloads, SECOND, args, rank, world)
+        blk2 = step_block(r2, args, world, peaks, peaks_src)
+        if rank == 0:
+            print(json.dumps({"workload": SECOND, "block": blk2}), flush=True)
+        return
     r = run_decode_step(torch, pa, workloads, HEADLINE, args, rank, world)
     blk = step_block(r, args, world, peaks, peaks_src)
     line = {"metric": METRIC, "value": blk.pop("value"), "unit": blk.pop("unit"),
@@ -964,10 +1004,22 @@ def ncu_case(args):
                     args.ncu_case]
         over = {"layers": 1, "pool_pages": None}
         case = workloads.config_case(name, device="cuda", **over)
-        part = workloads.CONFIGS[name].get("partition_tokens", 0)
+        cfg = workloads.CONFIGS[name]
+        part = cfg.get("partition_tokens", 0)
+        step = name in (HEADLINE, SECOND)  # the decode steps' call: the fused append
+        if step:
+            B = case.q.shape[1]
+            k_new, v_new = workloads.new_tokens(B, cfg["n_kv_heads"], cfg["head_dim"],
+                                                cfg["dtype"], seed=cfg["seed"] + 1,
+                                                device="cuda")
         for _ in range(args.warmup + args.steps):
-            pa.decode(case.q[0], case.k_cache, case.v_cache, case.block_table[0],
-                      case.ctx_lens, case.scale, partition_tokens=part)
+            if step:
+                pa.decode_append(case.q[0], k_new, v_new, case.k_cache, case.v_cache,
+                                 case.block_table[0], case.ctx_lens, case.scale,
+                                 partition_tokens=part)
+            else:
+                pa.decode(case.q[0], case.k_cache, case.v_cache, case.block_table[0],
+                          case.ctx_lens, case.scale, partition_tokens=part)
     torch.cuda.synchronize()
     assert pa.pa_last_device_error() == 0
 
@@ -978,6 +1030,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only-second", action="store_true",
+                    help="run only the LLaMA-7B-shaped decode step (for profiling)")
     ap.add_argument("--only-headline", action="store_true",
                     help="skip the second decode step and the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")

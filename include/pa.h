@@ -117,6 +117,36 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
               size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_append -- one decode step of the pages' serving loop in one
+ * call: the step's new K/V rows go into the cache and every query attends
+ * the whole context, new token included.
+ *
+ * For every sequence b with T = ctx_lens[b] >= 1 (T counts the new token):
+ *   1. the rows k_new[b][g], v_new[b][g] of every kv head g are stored at
+ *      position T - 1, page block_table[b][(T-1) / page_size], slot
+ *      (T-1) % page_size -- the per-step KV write of "吞吐与延迟的系统模型",
+ *      section 4 (2 L B d_kv b_kv bytes per step over all layers);
+ *   2. out[b] is what pa_decode computes over the T tokens.
+ * The result equals pa_append_kv (seq_idx = b, pos = T - 1) followed by
+ * pa_decode with the same arguments; one kernel does both: the CTA that
+ * reads the last page puts the new rows into its copy of that page, and one
+ * CTA per (sequence, kv head) writes them to the cache.  T = 0 writes zeros
+ * and stores nothing.
+ *   k_new, v_new  device, [batch][n_kv_heads][head_dim], dtype, 16-byte
+ *                 aligned
+ *   k_cache, v_cache  written in place (position T - 1 of every sequence)
+ * Every other argument, the workspace (pa_decode_workspace_size) and the
+ * plan are pa_decode's.  The page holding position T - 1 must be mapped in
+ * the table; a bad page id stores nothing and records PA_ERR_BAD_BLOCK.
+ */
+int pa_decode_append(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                     void *v_cache, const int32_t *block_table, const int32_t *ctx_lens,
+                     float *out, float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                     int page_size, int batch, int max_blocks_per_seq, int num_pages,
+                     pa_dtype dtype, int partition_tokens, void *workspace,
+                     size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_decode_window -- decode attention over an attention sink plus a sliding
  * window of recent keys (ch. 19 "推理系统与性能工程", KV-cache eviction: keep
  * the first tokens and the most recent window).

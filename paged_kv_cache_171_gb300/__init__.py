@@ -17,7 +17,8 @@ import ctypes
 import os
 
 __all__ = [
-    "PAError", "BF16", "F16", "lib", "dtype_code", "pa_decode",
+    "PAError", "BF16", "F16", "lib", "dtype_code", "pa_decode", "pa_decode_append",
+    "decode_append",
     "pa_decode_partition_tokens", "pa_decode_workspace_size",
     "pa_decode_static_workspace",
     "pa_merge_partials", "pa_append_kv", "pa_prefill_paged",
@@ -62,6 +63,8 @@ def lib():
         L.pa_strerror.restype = ctypes.c_char_p
         L.pa_decode.argtypes = [P, P, P, P, P, P, F] + [I] * 8 + [I, P, Z, P]
         L.pa_decode.restype = I
+        L.pa_decode_append.argtypes = [P] * 8 + [F] + [I] * 8 + [I, P, Z, P]
+        L.pa_decode_append.restype = I
         L.pa_decode_partition_tokens.argtypes = [I] * 7
         L.pa_decode_partition_tokens.restype = I
         L.pa_decode_workspace_size.argtypes = [I] * 7
@@ -166,6 +169,18 @@ def pa_decode(q, k_cache, v_cache, block_table, ctx_lens, out, scale, n_q_heads,
                          max_blocks_per_seq, num_pages, dtype, partition_tokens,
                          _ptr(workspace), workspace_bytes, _stream(stream))
     return _check(rc, "pa_decode")
+
+
+def pa_decode_append(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, out, scale,
+                     n_q_heads, n_kv_heads, head_dim, page_size, batch, max_blocks_per_seq,
+                     num_pages, dtype, partition_tokens=0, workspace=None, workspace_bytes=0,
+                     stream=None) -> int:
+    rc = lib().pa_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), _ptr(out),
+                                float(scale), n_q_heads, n_kv_heads, head_dim, page_size,
+                                batch, max_blocks_per_seq, num_pages, dtype, partition_tokens,
+                                _ptr(workspace), workspace_bytes, _stream(stream))
+    return _check(rc, "pa_decode_append")
 
 
 def pa_decode_static_workspace(q, k_cache, v_cache, block_table, ctx_lens, out,
@@ -407,6 +422,28 @@ def decode(q, k_cache, v_cache, block_table, ctx_lens, scale, partition_tokens=0
     pa_decode(q, k_cache, v_cache, block_table, ctx_lens, out, scale, hq, hkv, D, P,
               B, mb, pages, dtype_code(q), partition_tokens, workspace,
               ws_bytes, stream)
+    return out
+
+
+def decode_append(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, scale,
+                  partition_tokens=0, out=None, workspace=None, stream=None):
+    """pa_decode_append on tensors: q [B, h_q, D]; k_new, v_new [B, h_kv, D], the
+    step's token of each sequence, stored at position ctx_lens[b] - 1 (the
+    caches are written in place); ctx_lens counts that token.  Returns fp32
+    [B, h_q, D]."""
+    import torch
+    B, hq, D = q.shape
+    pages, hkv, P, D2 = k_cache.shape
+    assert D2 == D and block_table.shape[0] == B and tuple(k_new.shape) == (B, hkv, D)
+    mb = block_table.shape[1]
+    if out is None:
+        out = torch.empty((B, hq, D), dtype=torch.float32, device=q.device)
+    ws_bytes = pa_decode_workspace_size(B, hq, hkv, D, P, mb, partition_tokens)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes // 4, dtype=torch.float32, device=q.device)
+    pa_decode_append(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, out, scale, hq,
+                     hkv, D, P, B, mb, pages, dtype_code(q), partition_tokens, workspace,
+                     ws_bytes, stream)
     return out
 
 

@@ -395,7 +395,8 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache,
                 float scale, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
                 int batch, int max_blocks_per_seq, int num_pages, pa_dtype dtype,
                 int sink, int window, int partition_tokens, void *workspace,
-                size_t workspace_bytes, pa_stream_t stream) {
+                size_t workspace_bytes, pa_stream_t stream, const void *k_new = nullptr,
+                const void *v_new = nullptr) {
   if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !out)
     return PA_ERR_NULL;
   int rc = check_common(n_q_heads, n_kv_heads, head_dim, page_size, batch,
@@ -435,6 +436,8 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache,
   a.warp_parts = wp;
   a.sink = sink;
   a.window = window;
+  a.k_new = k_new;
+  a.v_new = v_new;
   return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 }  // namespace
@@ -451,6 +454,20 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
   return decode_impl(q, k_cache, v_cache, block_table, ctx_lens, out, scale, n_q_heads,
                      n_kv_heads, head_dim, page_size, batch, max_blocks_per_seq, num_pages,
                      dtype, 0, -1, partition_tokens, workspace, workspace_bytes, stream);
+}
+
+int pa_decode_append(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                     void *v_cache, const int32_t *block_table, const int32_t *ctx_lens,
+                     float *out, float scale, int n_q_heads, int n_kv_heads, int head_dim,
+                     int page_size, int batch, int max_blocks_per_seq, int num_pages,
+                     pa_dtype dtype, int partition_tokens, void *workspace,
+                     size_t workspace_bytes, pa_stream_t stream) {
+  if (!k_new || !v_new) return PA_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PA_ERR_ALIGN;
+  return decode_impl(q, k_cache, v_cache, block_table, ctx_lens, out, scale, n_q_heads,
+                     n_kv_heads, head_dim, page_size, batch, max_blocks_per_seq, num_pages,
+                     dtype, 0, -1, partition_tokens, workspace, workspace_bytes, stream, k_new,
+                     v_new);
 }
 
 int pa_decode_window(const void *q, const void *k_cache, const void *v_cache,

@@ -73,6 +73,11 @@ struct DecodeParams {
   // cascade decode, merged with the shared prefix's states afterwards).
   float *part;
   int part_stride, part_slot;
+  // Fused append (k_new set): the step's token of sequence b sits at
+  // position ctx_lens[b] - 1; its rows k_new/v_new [B][Hkv][D] are written
+  // into the cache at that position, and attended from there.
+  const uint16_t *k_new, *v_new;
+  uint16_t *k_cache, *v_cache;
 };
 
 // The keys a sequence's query attends, as a list of virtual pages.  Without
@@ -155,6 +160,11 @@ struct PageRing {
   int first, stride, n_i, num_pages, y_page, y_head;
   int ids_cur, ids_nxt;
   KeySet ks;  // chunk i is virtual page first + stride * i of this key set
+  // Fused append: logical page patch_lp (-1: none), row patch_row gets the
+  // step's token; lane l < 16 holds 16-byte chunk l of its K row, lane
+  // 16 + l chunk l of its V row.
+  int patch_lp, patch_row;
+  uint4 patch_val;
 
   // The raw table entry; checked only when it is used, so the load's latency
   // is hidden behind the 32 chunks that come first.
@@ -194,9 +204,24 @@ struct PageRing {
     }
   }
   // Warp-uniform wait for chunk i; on a timeout, records it, lets the other
-  // copies in flight land, and returns false.
+  // copies in flight land, and returns false.  The page holding a fused
+  // append's token gets the token's rows written over the copy (which may
+  // predate their write to the cache); the next copy into the stage is
+  // ordered after these stores by issue()'s proxy fence.
   __device__ bool wait(int i, int lane) {
-    if (__all_sync(kFull, mbar_wait(bar(i), parity(i)))) return true;
+    if (__all_sync(kFull, mbar_wait(bar(i), parity(i)))) {
+      if (patch_lp >= 0 && ks.logical(page(i)) == patch_lp) {
+        const int c = lane & 15;
+        if (c < D / 8) {
+          const uint32_t a = stage(i) + (lane >= 16 ? kPageBytes : 0) + swz(patch_row, c, 16);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(patch_val.x),
+                       "r"(patch_val.y), "r"(patch_val.z), "r"(patch_val.w)
+                       : "memory");
+        }
+        __syncwarp();
+      }
+      return true;
+    }
     if (lane == 0) record_error(status, PA_ERR_TIMEOUT);
     for (int j = i + 1; j < n_i && j < i + S; ++j) mbar_wait(bar(j), parity(j));
     return false;
@@ -576,6 +601,27 @@ __global__ void __launch_bounds__(NW * 32)
   ring.ks = ks;
   ring.y_page = p.n_kv_heads * 16;
   ring.y_head = g * 16;
+  ring.patch_lp = -1;
+  if (p.k_new && pg1 == n_pages) {
+    // Fused append: this CTA holds the last page, which holds key T - 1.
+    ring.patch_lp = (T - 1) >> 4;
+    ring.patch_row = (T - 1) & 15;
+    const int c = lane & 15;
+    const size_t src = (static_cast<size_t>(b) * p.n_kv_heads + g) * D + c * 8;
+    ring.patch_val = make_uint4(0u, 0u, 0u, 0u);
+    if (c < D / 8)
+      ring.patch_val = __ldg(reinterpret_cast<const uint4 *>((lane >= 16 ? p.v_new : p.k_new) + src));
+    if (warp == 0 && blockIdx.y % n_sub == 0) {
+      // one CTA per (sequence, kv head) writes the rows into the cache
+      int id = __ldg(ring.bt_row + ring.patch_lp);
+      if (static_cast<unsigned>(id) >= static_cast<unsigned>(p.num_pages)) {
+        if (lane == 0) record_error(p.status, PA_ERR_BAD_BLOCK);
+      } else if (c < D / 8) {
+        const size_t dst = ((static_cast<size_t>(id) * p.n_kv_heads + g) * 16 + ring.patch_row) * D + c * 8;
+        *reinterpret_cast<uint4 *>((lane >= 16 ? p.v_cache : p.k_cache) + dst) = ring.patch_val;
+      }
+    }
+  }
   ring.start(lane);
   for (int i = 0; i < S && i < ring.n_i; ++i) ring.issue(i, lane, &kmap, &vmap);
 
@@ -966,6 +1012,10 @@ int launch_decode_t(const DecodeLaunch &a, cudaStream_t stream) {
   p.part = a.part;
   p.part_stride = a.part_stride;
   p.part_slot = a.part_slot;
+  p.k_new = static_cast<const uint16_t *>(a.k_new);
+  p.v_new = static_cast<const uint16_t *>(a.v_new);
+  p.k_cache = static_cast<uint16_t *>(const_cast<void *>(a.k_cache));
+  p.v_cache = static_cast<uint16_t *>(const_cast<void *>(a.v_cache));
   const dim3 grid(gx, a.n_kv_heads * (p.group / GT), a.batch);
   if (split) {
     p.ctr = reinterpret_cast<int *>(reinterpret_cast<char *>(a.workspace) +

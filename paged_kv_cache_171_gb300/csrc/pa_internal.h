@@ -92,6 +92,10 @@ struct DecodeLaunch {
   // out (the own keys of a cascade decode).
   float *part = nullptr;
   int part_stride = 0, part_slot = 0;
+  // Fused append (plain decode only): the rows of each sequence's step token
+  // (position ctx_lens[b] - 1), [B][Hkv][head_dim], written into the cache
+  // (k_cache / v_cache are then written) and attended.
+  const void *k_new = nullptr, *v_new = nullptr;
 };
 
 constexpr int kDecodeWarps = 4;  // warps per decode CTA

@@ -740,8 +740,8 @@ def describe(name, cfg):
     pool = (f"shuffled pool of {cfg['pool_pages']} pages" if cfg.get("pool_pages")
             else "random block tables")
     qm = f", Q x {cfg['q_mul']:g}" if cfg.get("q_mul", 1.0) != 1.0 else ""
-    return (f"{name}: decode step of {cfg['layers']} layers x pa_decode_append (the step "
-            f"token's K/V write + decode), "
+    return (f"{name}: decode step of {cfg['layers']} layers (per layer the step token's K/V "
+            f"write, then attention over every cached token), "
             f"batch {cfg['batch']}, {cfg['n_q_heads']} q heads / {cfg['n_kv_heads']} kv "
             f"heads, head_dim {cfg['head_dim']}, {ctx_s}, {cfg['dtype']} KV, page_size "
             f"{cfg['page_size']}, {pool}{qm}")

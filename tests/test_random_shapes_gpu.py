@@ -60,6 +60,33 @@ def test_random_decode(seed):
 
 
 @pytest.mark.parametrize("seed", range(12))
+def test_random_decode_append(seed):
+    """pa_decode_append: each non-empty sequence's step token written at
+    position ctx - 1 (caches bit-exact), the decode over ctx tokens."""
+    rng = np.random.default_rng(7500 + seed)
+    kw = _case(rng, "decode")
+    cpu = workloads.paged_case(**kw)
+    B, hkv, D = len(kw["ctx"]), kw["n_kv_heads"], kw["head_dim"]
+    k_new, v_new = workloads.new_tokens(B, hkv, D, kw["dtype"], seed=int(rng.integers(1 << 30)))
+    seqs = [b for b in range(B) if kw["ctx"][b] > 0]
+    k_ref, v_ref = oracle.append_kv(k_new[seqs], v_new[seqs], cpu.k_cache, cpu.v_cache,
+                                    cpu.block_table[0], np.array(seqs, np.int32),
+                                    np.array([kw["ctx"][b] - 1 for b in seqs], np.int32))
+    ref = oracle.decode(cpu.q[0], k_ref.reshape(cpu.k_cache.shape),
+                        v_ref.reshape(cpu.v_cache.shape), cpu.block_table[0], cpu.ctx_lens,
+                        cpu.scale, cpu.dtype_code)
+    dev = to_device(workloads.paged_case(**kw), "cuda")
+    part = int(rng.choice([0, 16, 32, 64, 256, 512]))
+    out = pa.decode_append(dev.q[0], k_new.cuda(), v_new.cuda(), dev.k_cache, dev.v_cache,
+                           dev.block_table[0], dev.ctx_lens, dev.scale, partition_tokens=part)
+    torch.cuda.synchronize()
+    assert pa.pa_last_device_error() == 0
+    assert np.array_equal(oracle.bits(dev.k_cache), k_ref)
+    assert np.array_equal(oracle.bits(dev.v_cache), v_ref)
+    assert_close(out.cpu().numpy(), ref, f"decode_append {kw} part {part}")
+
+
+@pytest.mark.parametrize("seed", range(12))
 def test_random_prefill_and_split(seed):
     rng = np.random.default_rng(8000 + seed)
     n_new = int(rng.choice([1, 2, 3, 4, 8, int(rng.integers(1, 200))]))

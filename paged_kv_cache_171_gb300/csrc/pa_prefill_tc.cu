@@ -62,8 +62,8 @@
 // 2^-9 / sqrt(3) * rms(v) / 4.  The first tile of every row tile (l = 0)
 // and any tile that holds a new dominant key take two terms.  The four
 // warps of a softmax warpgroup vote per key tile: each posts its warp's
-// verdict and arrives on an mbarrier after the head terms of its first 32
-// keys, and reads the four verdicts after those of the first 64, so the
+// vote and arrives on an mbarrier after the head terms of its first 32
+// keys, and reads the four votes after those of the first 64, so the
 // vote's latency hides behind work that both modes share.  One thread tells the
 // MMA warp, which then issues the remainder's P V MMAs or not.  Long diffuse
 // rows take one term on most tiles: half the P V MMAs and half the P stores
@@ -529,7 +529,7 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
       m = mn;
       lp = __fmul2_rn(lp, make_float2(corr, corr));
     }
-    // ---- this row's verdict: one term of P for this key tile if the tile's
+    // ---- this row's vote: one term of P for this key tile if the tile's
     // largest weight 2^(cand - m) is below 1/16 of the weight of the earlier
     // tiles (NaN while m = -inf: two terms); the warpgroup votes below
     const bool fine = 16.f * ex2(cand - m) < lp.x + lp.y;
@@ -607,8 +607,8 @@ __device__ __forceinline__ void softmax_tiles(uint32_t sb, uint32_t tmem, const 
       tile_p(std::integral_constant<int, 2>{}, 0);
     } else {
       // Keys 0-63: head terms first (both modes need them; the weights stay
-      // in s for a remainder), the warp's verdict posted after the first 32
-      // and the four verdicts read after all 64, so that neither the vote's
+      // in s for a remainder), the warp's vote posted after the first 32
+      // and the four votes read after all 64, so that neither the vote's
       // latency nor a branch on its outcome holds up the exponentials.
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {

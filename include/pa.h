@@ -137,7 +137,10 @@ int pa_decode(const void *q, const void *k_cache, const void *v_cache,
  *   k_cache, v_cache  written in place (position T - 1 of every sequence)
  * Every other argument, the workspace (pa_decode_workspace_size) and the
  * plan are pa_decode's.  The page holding position T - 1 must be mapped in
- * the table; a bad page id stores nothing and records PA_ERR_BAD_BLOCK.
+ * the table; a bad page id stores nothing and records PA_ERR_BAD_BLOCK.  As
+ * with pa_append_kv, no two sequences may place their token at the same
+ * (page, slot): a page that forks of a shared prefix still share is copied
+ * first (pa_pool_prepare_append, pa_copy_pages).
  */
 int pa_decode_append(const void *q, const void *k_new, const void *v_new, void *k_cache,
                      void *v_cache, const int32_t *block_table, const int32_t *ctx_lens,

@@ -543,7 +543,8 @@ __global__ void __launch_bounds__(NW * 32)
 
   int T = p.ctx_lens[b];
   const int maxT = p.max_blocks * 16;
-  if (T < 0 || T > maxT) {
+  const bool t_ok = T >= 0 && T <= maxT;  // a clamped length stores no token
+  if (!t_ok) {
     if (tid == 0) record_error(p.status, PA_ERR_BAD_CTX);
     T = T < 0 ? 0 : maxT;
   }
@@ -607,18 +608,19 @@ __global__ void __launch_bounds__(NW * 32)
     ring.patch_lp = (T - 1) >> 4;
     ring.patch_row = (T - 1) & 15;
     const int c = lane & 15;
-    const size_t src = (static_cast<size_t>(b) * p.n_kv_heads + g) * D + c * 8;
+    const uint16_t *src = (lane >= 16 ? p.v_new : p.k_new) +
+                          (static_cast<size_t>(b) * p.n_kv_heads + g) * D + c * 8;
     ring.patch_val = make_uint4(0u, 0u, 0u, 0u);
-    if (c < D / 8)
-      ring.patch_val = __ldg(reinterpret_cast<const uint4 *>((lane >= 16 ? p.v_new : p.k_new) + src));
-    if (warp == 0 && blockIdx.y % n_sub == 0) {
+    if (c < D / 8) ring.patch_val = __ldg(reinterpret_cast<const uint4 *>(src));
+    if (t_ok && warp == 0 && blockIdx.y % n_sub == 0) {
       // one CTA per (sequence, kv head) writes the rows into the cache
       int id = __ldg(ring.bt_row + ring.patch_lp);
       if (static_cast<unsigned>(id) >= static_cast<unsigned>(p.num_pages)) {
         if (lane == 0) record_error(p.status, PA_ERR_BAD_BLOCK);
       } else if (c < D / 8) {
-        const size_t dst = ((static_cast<size_t>(id) * p.n_kv_heads + g) * 16 + ring.patch_row) * D + c * 8;
-        *reinterpret_cast<uint4 *>((lane >= 16 ? p.v_cache : p.k_cache) + dst) = ring.patch_val;
+        const size_t row = (static_cast<size_t>(id) * p.n_kv_heads + g) * 16 + ring.patch_row;
+        *reinterpret_cast<uint4 *>((lane >= 16 ? p.v_cache : p.k_cache) + row * D + c * 8) =
+            ring.patch_val;
       }
     }
   }

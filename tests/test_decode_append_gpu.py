@@ -114,6 +114,24 @@ def test_decode_append_empty_sequence_and_bad_page():
     assert torch.equal(dev.k_cache, before_k) and torch.equal(dev.v_cache, before_v)
 
 
+def test_decode_append_context_beyond_the_table():
+    """A context length past the table is reported (PA_ERR_BAD_CTX) and stores
+    no token; the other sequences store theirs."""
+    cpu = _case(128, 16, 4, "bf16", [40, 40], seed=69)
+    dev = to_device(cpu, "cuda")
+    before_k, before_v = dev.k_cache.clone(), dev.v_cache.clone()
+    dev.ctx_lens[0] = dev.block_table.shape[2] * 16 + 5
+    k_new, v_new = workloads.new_tokens(2, 4, 128, "bf16", seed=70, device="cuda")
+    pa.decode_append(dev.q[0], k_new, v_new, dev.k_cache, dev.v_cache, dev.block_table[0],
+                     dev.ctx_lens, dev.scale)
+    assert pa.pa_last_device_error() == -12  # PA_ERR_BAD_CTX
+    page, slot = int(dev.block_table[0, 1, 40 // 16]), 40 % 16
+    assert torch.equal(dev.k_cache[page, :, slot], k_new[1])
+    dev.k_cache[page, :, slot] = before_k[page, :, slot]
+    dev.v_cache[page, :, slot] = before_v[page, :, slot]
+    assert torch.equal(dev.k_cache, before_k) and torch.equal(dev.v_cache, before_v)
+
+
 def test_decode_append_llama_layer_sampled_sequences():
     """The LLaMA-7B-shaped layer at full size (8 sequences x 4096 tokens, 32
     heads, bf16), the step's token at position 4095: two sequences against

@@ -153,3 +153,27 @@ def test_decode_append_llama_layer_sampled_sequences():
     ref = oracle.decode(q, k, v, table, ctx, case.scale, case.dtype_code)
     sel = torch.tensor(seqs, device="cuda")
     assert_close(out.index_select(0, sel).cpu().numpy(), ref, "decode_append llama layer")
+
+
+def test_decode_append_ragged_gqa_layer_sampled_sequences():
+    """One layer of the ragged GQA-4 batch at full size (64 sequences of
+    128-8192 tokens, 32/8 heads, bf16, Q x 2, the automatic split plan): every
+    sequence's new rows land at position ctx - 1; the shortest, the longest and
+    one more sequence against the oracle over the updated pages."""
+    case = workloads.config_case("gqa4_b64_ragged", device="cuda", layers=1, pool_pages=None)
+    B = case.q.shape[1]
+    k_new, v_new = workloads.new_tokens(B, 8, 128, "bf16", seed=71, device="cuda")
+    out = pa.decode_append(case.q[0], k_new, v_new, case.k_cache, case.v_cache,
+                           case.block_table[0], case.ctx_lens, case.scale)
+    torch.cuda.synchronize()
+    assert pa.pa_last_device_error() == 0
+    pos = (case.ctx_lens - 1).long()
+    pages = case.block_table[0].gather(1, (pos // 16).view(B, 1)).view(B).long()
+    assert torch.equal(case.k_cache[pages, :, pos % 16], k_new)
+    assert torch.equal(case.v_cache[pages, :, pos % 16], v_new)
+    lens = case.ctx_lens.cpu()
+    seqs = sorted({int(lens.argmin()), int(lens.argmax()), 17})
+    q, k, v, table, ctx = compact_host_copy(case, 0, seqs)
+    ref = oracle.decode(q, k, v, table, ctx, case.scale, case.dtype_code)
+    sel = torch.tensor(seqs, device="cuda")
+    assert_close(out.index_select(0, sel).cpu().numpy(), ref, "decode_append ragged GQA layer")

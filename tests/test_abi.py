@@ -82,6 +82,29 @@ def test_decode_rejects_bad_arguments(L, kw, code):
     assert _decode(L, **kw) == code
 
 
+def _decode_append(L, kn=FAKE, vn=FAKE, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, ctx=FAKE, out=FAKE, scale=0.1,
+             hq=32, hkv=8, d=128, p=16, b=2, mb=8, pages=16, dtype=0, pt=0,
+             ws=None, wsb=0)
+    a.update(kw)
+    return L.pa_decode_append(a["q"], kn, vn, a["k"], a["v"], a["bt"], a["ctx"], a["out"],
+                              ctypes.c_float(a["scale"]), a["hq"], a["hkv"], a["d"], a["p"],
+                              a["b"], a["mb"], a["pages"], a["dtype"], a["pt"], a["ws"],
+                              a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kn=None), -1), (dict(vn=None), -1), (dict(q=None), -1), (dict(k=None), -1),
+    (dict(kn=FAKE + 8), -8), (dict(vn=FAKE + 2), -8), (dict(v=FAKE + 4), -8),
+    (dict(hq=30, hkv=8), -2), (dict(d=96), -3), (dict(p=8), -4), (dict(b=0), -5),
+    (dict(dtype=2), -6), (dict(pt=24), -9), (dict(pt=16, ws=None, wsb=0), -7),
+])
+def test_decode_append_rejects_bad_arguments(L, kw, code):
+    """The fused step checks its new-token pointers, then everything pa_decode
+    checks, before any CUDA call."""
+    assert _decode_append(L, **kw) == code
+
+
 def _group_tile(group):
     return 8 if group % 8 == 0 else 4 if group % 4 == 0 else 2 if group % 2 == 0 else 1
 

@@ -141,3 +141,32 @@ def test_random_topm(seed):
         assert np.array_equal(keep.cpu().numpy().astype(bool), want), (L, H, N, budget)
         assert np.array_equal(per_head.cpu().numpy(), want.sum(axis=2)), (L, H, N, budget)
     assert pa.pa_last_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_cascade(seed):
+    """pa_decode_cascade on random fork counts, prefix and own lengths (page
+    and tile edges included), heads, head dims, dtypes and range sizes,
+    against the oracle on each fork's concatenated sequence."""
+    import math
+    from tests.test_cascade_gpu import _case as cascade_case, _oracle as cascade_oracle
+    rng = np.random.default_rng(9500 + seed)
+    hq, hkv = HEADS[rng.integers(len(HEADS))]
+    D, dtype = int(rng.choice([64, 128])), str(rng.choice(["bf16", "fp16"]))
+    B = int(rng.integers(1, 13))
+    edges = [1, 15, 16, 17, 127, 128, 129, 511, 512, 513]
+    prefix_len = int(rng.choice(edges)) if rng.random() < 0.5 else int(rng.integers(1, 1500))
+    own = [int(rng.choice([0, 1, 15, 16, 17])) if rng.random() < 0.4
+           else int(rng.integers(0, 200)) for _ in range(B)]
+    part = int(rng.choice([0, 128, 256, 512]))
+    q, kc, vc, ptab, tab, ctx = cascade_case(B, hq, hkv, D, dtype, prefix_len, own,
+                                             seed=int(rng.integers(1 << 30)))
+    scale = 1.0 / math.sqrt(D)
+    ref = cascade_oracle(q, kc, vc, ptab, prefix_len, tab, own, scale,
+                         workloads.DTYPE_CODE[dtype])
+    out = pa.decode_cascade(q.cuda(), kc.cuda(), vc.cuda(), ptab.cuda(), prefix_len,
+                            tab.cuda(), ctx.cuda(), scale, partition_tokens=part)
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), ref,
+                 f"cascade B={B} {hq}/{hkv} D={D} {dtype} prefix {prefix_len} own {own} part {part}")
+    assert pa.pa_last_device_error() == 0

@@ -16,13 +16,19 @@
 // equals S*.  The kept candidates are then exactly: f < S*, plus the first r
 // with f = S* in index order.
 //
-// Only two passes stream the scores.  The first histograms the top 11 bits
-// and a one-CTA pick finds the bucket b1 holding the K-th key.  The second
-// settles every element outside b1 (kept if its bucket is below b1, dropped
-// if above), writes the keep mask and appends the (index, key) of b1's
-// elements to a candidate list.  The remaining digits, the tie rank and the
-// final keeps then run over the candidates alone:
-// the r-th tie is located by counting ties per chunk of the array, scanning
+// One pass streams the scores when a sample can name the first digit.  A
+// histogram of the top 11 bits over every 32nd chunk of the array, and a
+// one-CTA pick, name the bucket b1 that holds the K-th key -- if the K-th
+// sample lies more than six standard deviations of its sampling error from
+// both edges of its bucket.  The split pass then settles every element
+// outside b1 (kept if its bucket is below b1, dropped if above), writes the
+// keep mask, appends the (index, key) of b1's elements to a candidate list,
+// and counts the kept elements below b1 exactly; b1 is confirmed when the
+// K-th key falls among b1's candidates by those counts.  Otherwise (the
+// sample unsure, or wrong) the exact first digit runs: a histogram over every
+// element, its pick, and the split pass again.  Arrays under 512 chunks take
+// the exact first digit directly.  The remaining digits, the tie rank and the
+// final keeps then run over the candidates alone: the r-th tie is located by counting ties per chunk of the array, scanning
 // the counts to find its chunk, and ranking that one chunk's ties; with its
 // index idx*, a candidate is kept when (f, index) <= (S*, idx*).
 #include "pa_device.cuh"
@@ -37,6 +43,7 @@ constexpr int kChunk = kThreads * kPerThread;      // elements per chunk (final 
 
 constexpr int kBins1 = 2048, kBins2 = 2048, kBins3 = 1024;  // digits of 11, 11, 10 bits
 constexpr int kShift1 = 21, kShift2 = 10;
+constexpr int kSampleStep = 32;  // the first-digit sample: every 32nd chunk
 
 // The state of the select, in the workspace after the histograms.
 struct TopmState {
@@ -47,8 +54,16 @@ struct TopmState {
   uint32_t tie_rank;   // its 1-based rank among that chunk's ties
   uint32_t idx_star;   // its index: the last kept candidate
   uint32_t n_cand;     // elements of bucket b1 appended to the candidate list
+  uint32_t kept_below; // kept candidates of buckets below b1 (the split pass)
+  uint32_t sure;       // 1: b1 named by the sample (the split pass ran on it)
+  uint32_t redo;       // 1: b1 not confirmed; the exact first digit runs
+  uint32_t k_total;    // K, the candidates to keep
   uint32_t pad;
 };
+static_assert(sizeof(TopmState) % 16 == 0, "the tie counts follow, 16-byte aligned");
+static_assert(offsetof(TopmState, n_cand) % 8 == 0 &&
+                  offsetof(TopmState, kept_below) == offsetof(TopmState, n_cand) + 4,
+              "n_cand and kept_below are the low and high words of one 64-bit counter");
 
 // Ascending f <=> descending score; -0.0 as 0.0; NaN after every number.
 __device__ __forceinline__ uint32_t score_key(float s) {
@@ -71,7 +86,8 @@ __global__ void __launch_bounds__(kThreads)
   for (int i = blockIdx.x * kThreads + threadIdx.x; i < n_chunks; i += stride) tiecnt[i] = 0;
   if (per_head)
     for (int i = blockIdx.x * kThreads + threadIdx.x; i < n_rows; i += stride) per_head[i] = 0;
-  if (blockIdx.x == 0 && threadIdx.x == 0) *st = TopmState{0u, 0u, k, 0u, 0u, 0u, 0u, 0u};
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    *st = TopmState{0u, 0u, k, 0u, 0u, 0u, 0u, 0u, 0u, 0u, k, 0u};
 }
 
 // The kPerThread consecutive scores from `base` (16-byte aligned when the
@@ -120,22 +136,36 @@ __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v) {
   return v + (wid > 0 ? wsum[wid - 1] : 0u);
 }
 
-// First digit: histogram of the top 11 key bits over every candidate
-// element.  Each quarter of the CTA's warps counts into its own copy in
-// shared memory (fewer collisions on the few crowded bins), summed at the end.
+// First digit: histogram of the top 11 key bits over the candidate elements
+// of every `step`-th chunk (32: the sample; 1: every element).  Each quarter
+// of the CTA's warps counts into its own copy in shared memory (fewer
+// collisions on the few crowded bins), summed at the end.  gated: the exact
+// pass after the split, run only when the split pass's counts do not confirm
+// the sampled b1 (every CTA decides alike from fields no kernel of this step
+// writes; CTA 0 records it, and the remaining rank when confirmed).
 __global__ void __launch_bounds__(kThreads)
     topm_hist1_kernel(const float *__restrict__ scores, int n, int N, int current,
-                      uint32_t *__restrict__ hist) {
+                      uint32_t *__restrict__ hist, int step, TopmState *__restrict__ st,
+                      int gated) {
   griddep_wait();  // the previous launch of the stream has completed
   griddep_release();
+  if (gated) {
+    const uint32_t K = st->k_total, below = st->kept_below, nc = st->n_cand;
+    const bool ok = st->sure && below < K && K <= below + nc;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      st->redo = ok ? 0u : 1u;
+      st->k_rem = ok ? K - below : K;
+    }
+    if (ok) return;
+  }
   constexpr int kCopies = 4;
   __shared__ uint32_t h[kCopies][kBins1];
   for (int i = threadIdx.x; i < kCopies * kBins1; i += kThreads) h[i / kBins1][i % kBins1] = 0;
   __syncthreads();
   uint32_t *mine = h[(threadIdx.x >> 5) & (kCopies - 1)];
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kChunk;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kChunk * step;
   float nx[kPerThread];  // the next chunk's run, loaded while this one is counted
-  int64_t cbase = static_cast<int64_t>(blockIdx.x) * kChunk;
+  int64_t cbase = static_cast<int64_t>(blockIdx.x) * kChunk * step;
   if (cbase < n) load_run(scores, n, static_cast<int>(cbase) + threadIdx.x * kPerThread, nx);
   for (; cbase < n; cbase += stride) {
     const int base = static_cast<int>(cbase) + threadIdx.x * kPerThread;
@@ -175,11 +205,26 @@ __global__ void __launch_bounds__(kThreads)
 
 // One CTA of 1024 threads: the bin of `hist` (BINS bins, digit at `shift`)
 // holding the k_rem-th key of the current bucket; clears the histogram.
+// gated (the exact first digit): only when the sampled b1 was not confirmed,
+// after clearing what the split pass on it counted.
 template <int BINS>
 __global__ void __launch_bounds__(1024)
-    topm_pick_kernel(uint32_t *__restrict__ hist, TopmState *__restrict__ st, int shift) {
+    topm_pick_kernel(uint32_t *__restrict__ hist, TopmState *__restrict__ st, int shift,
+                     int gated, int32_t *__restrict__ per_head, int n_rows) {
   griddep_wait();  // the previous launch of the stream has completed
   griddep_release();
+  if (gated) {
+    if (!st->redo) return;
+    if (per_head)
+      for (int i = threadIdx.x; i < n_rows; i += 1024) per_head[i] = 0;
+    if (threadIdx.x == 0) {
+      st->n_cand = 0u;
+      st->kept_below = 0u;
+      st->prefix = 0u;
+      st->mask = 0u;
+    }
+    __syncthreads();
+  }
   constexpr int kPer = BINS / 1024;
   const int t = threadIdx.x;
   uint32_t v[kPer], sum = 0;
@@ -206,20 +251,67 @@ __global__ void __launch_bounds__(1024)
   for (int i = 0; i < kPer; ++i) hist[kPer * t + i] = 0;
 }
 
+// One CTA of 1024 threads: b1 from the sample histogram (kBins1 bins) when
+// the K-th key's place among the sampled candidates, K_s = K n_s / n_c, lies
+// more than 6 sigma + 4 (sigma^2 = K_s (1 - K_s / n_s), the binomial
+// sampling error) inside its bucket; clears the histogram.  Single precision
+// and one thread for the bounds: a bin qualifies when its cumulative counts
+// satisfy before < K_s - margin and after >= K_s + margin, which at most one
+// bin does (the conversions to float keep the counts' order).
+__global__ void __launch_bounds__(1024)
+    topm_pick_sample_kernel(uint32_t *__restrict__ hist, TopmState *__restrict__ st,
+                            float n_cands) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
+  constexpr int kPer = kBins1 / 1024;
+  const int t = threadIdx.x;
+  uint32_t v[kPer], sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    v[i] = hist[kPer * t + i];
+    sum += v[i];
+  }
+  const uint32_t incl = block_scan_incl<1024>(sum);
+  __shared__ float s_lo, s_hi;
+  if (t == 1023) {
+    const float ns = static_cast<float>(incl);
+    const float ks = static_cast<float>(st->k_total) * ns / n_cands;
+    const float margin = 6.f * sqrtf(fmaxf(ks * (1.f - ks / fmaxf(ns, 1.f)), 0.f)) + 4.f;
+    s_lo = incl >= 4096u ? ks - margin : -1.f;  // too small a sample: no bin
+    s_hi = ks + margin;
+  }
+  __syncthreads();
+  const float lo = s_lo, hi = s_hi;
+  uint32_t before = incl - sum;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t after = before + v[i];
+    if (static_cast<float>(before) < lo && static_cast<float>(after) >= hi) {
+      st->prefix = static_cast<uint32_t>(kPer * t + i) << kShift1;
+      st->mask = static_cast<uint32_t>(kBins1 - 1) << kShift1;
+      st->sure = 1u;
+    }
+    before = after;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) hist[kPer * t + i] = 0;
+}
+
 // Second pass over the scores.  Every element outside bucket b1 is settled:
 // kept (current position, or a bucket below b1) or dropped; b1's elements
 // are written 0 here and appended to the candidate list.  Kept rows per
-// (layer, head) are summed in shared memory, then added once per CTA.
-__global__ void __launch_bounds__(kThreads, 8)
-    topm_split_kernel(const float *__restrict__ scores, int n, int N, int current,
-                      TopmState *__restrict__ st, uint8_t *__restrict__ keep,
-                      int32_t *__restrict__ per_head, uint32_t *__restrict__ cand,
-                      uint32_t *__restrict__ ckey) {
-  griddep_wait();  // the previous launch of the stream has completed
-  griddep_release();
+// (layer, head) are summed in shared memory, then added once per CTA; so are
+// the kept elements of buckets below b1 (current positions excepted), in the
+// high word of the same 64-bit atomic that reserves the CTA's candidate slots.
+__device__ __forceinline__ void split_chunk(const float *__restrict__ scores, int n, int N,
+                                            int current, uint32_t b1, int cbase,
+                                            TopmState *__restrict__ st,
+                                            uint8_t *__restrict__ keep,
+                                            int32_t *__restrict__ per_head,
+                                            uint32_t *__restrict__ cand,
+                                            uint32_t *__restrict__ ckey) {
   __shared__ int cnt[kChunk + 2];  // rows of this chunk, relative to its first
-  const uint32_t b1 = st->prefix >> kShift1;
-  const int cbase = blockIdx.x * kChunk;
+  __shared__ uint32_t wsum[kThreads / 32 + 1], wbel[kThreads / 32];
   const int row0 = static_cast<int>(static_cast<unsigned>(cbase) / static_cast<unsigned>(N));
   const int cend = min(n, cbase + kChunk);
   const int n_rows =
@@ -233,7 +325,9 @@ __global__ void __launch_bounds__(kThreads, 8)
   load_run(scores, n, base, sc);
   const int t0 = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
   const int r0 = static_cast<int>(static_cast<unsigned>(base) / static_cast<unsigned>(N)) - row0;
-  uint32_t kbits = 0, cbits = 0;  // bit e: element base + e is kept / a candidate
+  // bit e (e < 16): element base + e is kept / a candidate; bits 16..: the
+  // kept candidates (not current positions) below b1
+  uint32_t kbits = 0, cbits = 0;
   if (base + kPerThread <= n && N >= kPerThread) {
     // Whole run, at most one row boundary (at element N - t0 when t0 + 16 > N):
     // decisions as bit masks, no per-element branches.
@@ -247,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, 8)
       kbits |= static_cast<uint32_t>(bk < b1) << e;
       cbits |= static_cast<uint32_t>(bk == b1) << e;
     }
+    cbits = (cbits & ~cur) | static_cast<uint32_t>(__popc(kbits & ~cur)) << kPerThread;
     kbits |= cur;
-    cbits &= ~cur;
     uint4 w;  // bit e of kbits -> byte e
     w.x = ((kbits & 15u) * 0x00204081u) & 0x01010101u;
     w.y = (((kbits >> 4) & 15u) * 0x00204081u) & 0x01010101u;
@@ -271,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 8)
       const uint32_t bk = score_key(sc[e]) >> kShift1;
       const bool k = t == current || bk < b1;
       if (t != current && bk == b1) cbits |= 1u << e;
+      if (t != current && bk < b1) cbits += 1u << kPerThread;
       kbits |= static_cast<uint32_t>(k) << e;
       keep[base + e] = k ? 1u : 0u;
       if (per_head && k) {
@@ -288,9 +383,11 @@ __global__ void __launch_bounds__(kThreads, 8)
     }
     if (per_head && run) atomicAdd(&cnt[run_row], run);
   }
-  // append the candidates in index order: one atomic per CTA
-  __shared__ uint32_t wsum[kThreads / 32 + 1];
+  // append the candidates in index order and add the kept-below count: one
+  // 64-bit atomic per CTA (candidates in the low word, which cannot carry)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t wbelow = __reduce_add_sync(0xffffffffu, cbits >> kPerThread);
+  cbits &= (1u << kPerThread) - 1u;
   const uint32_t mine = __popc(cbits);
   uint32_t incl = mine;
 #pragma unroll
@@ -298,16 +395,24 @@ __global__ void __launch_bounds__(kThreads, 8)
     const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += u;
   }
-  if (lane == 31) wsum[warp] = incl;
+  if (lane == 31) {
+    wsum[warp] = incl;
+    wbel[warp] = wbelow;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t tot = 0;
+    uint32_t tot = 0, bel = 0;
     for (int w = 0; w < kThreads / 32; ++w) {
       const uint32_t v = wsum[w];
       wsum[w] = tot;
       tot += v;
+      bel += wbel[w];
     }
-    wsum[kThreads / 32] = tot ? atomicAdd(&st->n_cand, tot) : 0u;
+    const unsigned long long add = static_cast<unsigned long long>(bel) << 32 | tot;
+    wsum[kThreads / 32] =
+        add ? static_cast<uint32_t>(atomicAdd(
+                  reinterpret_cast<unsigned long long *>(&st->n_cand), add))
+            : 0u;
   }
   __syncthreads();
   uint32_t pos = wsum[kThreads / 32] + wsum[warp] + incl - mine;
@@ -319,6 +424,40 @@ __global__ void __launch_bounds__(kThreads, 8)
   if (per_head) {
     for (int i = threadIdx.x; i < n_rows; i += kThreads)
       if (cnt[i]) atomicAdd(per_head + row0 + i, cnt[i]);
+  }
+}
+
+// The split pass, one CTA per chunk.  gate 0: always; 1: on the sampled b1,
+// if the sample named one.
+__global__ void __launch_bounds__(kThreads, 8)
+    topm_split_kernel(const float *__restrict__ scores, int n, int N, int current,
+                      TopmState *__restrict__ st, uint8_t *__restrict__ keep,
+                      int32_t *__restrict__ per_head, uint32_t *__restrict__ cand,
+                      uint32_t *__restrict__ ckey, int gate) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
+  if (gate == 1 && !st->sure) return;
+  split_chunk(scores, n, N, current, st->prefix >> kShift1, blockIdx.x * kChunk, st, keep,
+              per_head, cand, ckey);
+}
+
+// The split pass on the exact b1, only if the sampled one was not confirmed:
+// a grid-stride loop over the chunks, so that the usual case (nothing to do)
+// costs a small grid.
+__global__ void __launch_bounds__(kThreads, 8)
+    topm_split_redo_kernel(const float *__restrict__ scores, int n, int N, int current,
+                           TopmState *__restrict__ st, uint8_t *__restrict__ keep,
+                           int32_t *__restrict__ per_head, uint32_t *__restrict__ cand,
+                           uint32_t *__restrict__ ckey) {
+  griddep_wait();  // the previous launch of the stream has completed
+  griddep_release();
+  if (!st->redo) return;
+  const uint32_t b1 = st->prefix >> kShift1;
+  for (int64_t cbase = static_cast<int64_t>(blockIdx.x) * kChunk; cbase < n;
+       cbase += static_cast<int64_t>(gridDim.x) * kChunk) {
+    split_chunk(scores, n, N, current, b1, static_cast<int>(cbase), st, keep, per_head, cand,
+                ckey);
+    __syncthreads();  // the shared counts are reused by the next chunk
   }
 }
 
@@ -608,18 +747,48 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
   const int n_rows = n_layers * n_heads;
   cudaError_t e = launch_pdl(topm_init_kernel, dim3(sms), T, 0, s, hist1, n_zero, tiecnt,
                              n_chunks, kept_per_head, n_rows, st, static_cast<uint32_t>(k));
-  if (e == cudaSuccess)
-    e = launch_pdl(topm_hist1_kernel, dim3(grid), T, 0, s, scores, ni, n_tokens, current, hist1);
-  if (e == cudaSuccess) e = launch_pdl(topm_pick_kernel<kBins1>, one, T1k, 0, s, hist1, st, kShift1);
-  if (e == cudaSuccess)
-    e = launch_pdl(topm_split_kernel, dim3(n_chunks), T, 0, s, scores, ni, n_tokens, current, st,
-                   keep, kept_per_head, cand, ckey);
+  int32_t *const no_rows = nullptr;
+  if (n_chunks >= kSampleStep * 16) {
+    // the sampled first digit; the exact one behind it, gated on the counts
+    const int n_sampled = (n_chunks + kSampleStep - 1) / kSampleStep;
+    const int sgrid = n_sampled < sms * 4 ? n_sampled : sms * 4;
+    if (e == cudaSuccess)
+      e = launch_pdl(topm_hist1_kernel, dim3(sgrid), T, 0, s, scores, ni, n_tokens, current,
+                     hist1, kSampleStep, st, 0);
+    if (e == cudaSuccess)
+      e = launch_pdl(topm_pick_sample_kernel, one, T1k, 0, s, hist1, st,
+                     static_cast<float>(n_cand));
+    if (e == cudaSuccess)
+      e = launch_pdl(topm_split_kernel, dim3(n_chunks), T, 0, s, scores, ni, n_tokens, current,
+                     st, keep, kept_per_head, cand, ckey, 1);
+    if (e == cudaSuccess)
+      e = launch_pdl(topm_hist1_kernel, dim3(grid), T, 0, s, scores, ni, n_tokens, current,
+                     hist1, 1, st, 1);
+    if (e == cudaSuccess)
+      e = launch_pdl(topm_pick_kernel<kBins1>, one, T1k, 0, s, hist1, st, kShift1, 1,
+                     kept_per_head, n_rows);
+    if (e == cudaSuccess)
+      e = launch_pdl(topm_split_redo_kernel, dim3(grid), T, 0, s, scores, ni, n_tokens, current,
+                     st, keep, kept_per_head, cand, ckey);
+  } else {
+    if (e == cudaSuccess)
+      e = launch_pdl(topm_hist1_kernel, dim3(grid), T, 0, s, scores, ni, n_tokens, current,
+                     hist1, 1, st, 0);
+    if (e == cudaSuccess)
+      e = launch_pdl(topm_pick_kernel<kBins1>, one, T1k, 0, s, hist1, st, kShift1, 0, no_rows,
+                     0);
+    if (e == cudaSuccess)
+      e = launch_pdl(topm_split_kernel, dim3(n_chunks), T, 0, s, scores, ni, n_tokens, current,
+                     st, keep, kept_per_head, cand, ckey, 0);
+  }
   if (e == cudaSuccess)
     e = launch_pdl(topm_cand_hist_kernel<2>, dim3(cgrid), T, 0, s, cand, ckey, st, hist2);
-  if (e == cudaSuccess) e = launch_pdl(topm_pick_kernel<kBins2>, one, T1k, 0, s, hist2, st, kShift2);
+  if (e == cudaSuccess)
+    e = launch_pdl(topm_pick_kernel<kBins2>, one, T1k, 0, s, hist2, st, kShift2, 0, no_rows, 0);
   if (e == cudaSuccess)
     e = launch_pdl(topm_cand_hist_kernel<3>, dim3(cgrid), T, 0, s, cand, ckey, st, hist3);
-  if (e == cudaSuccess) e = launch_pdl(topm_pick_kernel<kBins3>, one, T1k, 0, s, hist3, st, 0);
+  if (e == cudaSuccess)
+    e = launch_pdl(topm_pick_kernel<kBins3>, one, T1k, 0, s, hist3, st, 0, 0, no_rows, 0);
   if (e == cudaSuccess)
     e = launch_pdl(topm_cand_tie_kernel, dim3(cgrid), T, 0, s, cand, ckey, st, tiecnt);
   if (e == cudaSuccess) e = launch_pdl(topm_scan_kernel, one, T1k, 0, s, tiecnt, n_chunks, st);

@@ -90,3 +90,64 @@ def test_topm_all_scores_equal():
         assert np.array_equal(keep.cpu().numpy().astype(bool), want), budget
         assert np.array_equal(per_head.cpu().numpy(), want.sum(axis=2)), budget
     assert pa.pa_last_device_error() == 0
+
+
+def _first_digit_path(ws):
+    """(sure, redo) from the select's state in the workspace (after the three
+    histograms of 2048, 2048 and 1024 counts): sure = the 1/32 chunk sample
+    named the first digit's bucket, redo = the exact first digit ran."""
+    w = ws.cpu().numpy().view(np.uint32)
+    state = w[(2048 + 2048 + 1024):][:12]
+    return int(state[8]), int(state[9])
+
+
+def _retain_large(s, current, budget):
+    L, H, N = s.shape
+    dev = torch.from_numpy(s).cuda()
+    ws = torch.empty(pa.pa_topm_workspace_size(L, H, N) // 4, dtype=torch.int32, device="cuda")
+    keep, per_head = pa.topm_retain(dev, current, budget, workspace=ws)
+    torch.cuda.synchronize()
+    assert pa.pa_last_device_error() == 0
+    want = oracle.topm_retain(s, current, budget)
+    got = keep.cpu().numpy().astype(bool)
+    assert np.array_equal(got, want), int((got != want).sum())
+    assert np.array_equal(per_head.cpu().numpy(), want.sum(axis=2))
+    return _first_digit_path(ws)
+
+
+def test_topm_sample_confirmed():
+    """8 x 8 x 65536 normal scores, a quarter kept: the sample names the
+    threshold's first-digit bucket and the split pass confirms it."""
+    s = _scores(8, 8, 65536, 73)
+    assert _retain_large(s, 65535, s.size // 4) == (1, 0)
+
+
+def test_topm_sample_misled():
+    """The sampled chunks (every 32nd run of 4096 scores) hold scores 3 higher
+    than the rest: the sample names a bucket far above the true threshold with
+    full confidence, the split pass's counts refute it, and the exact first
+    digit runs; the kept set is still exact."""
+    s = _scores(8, 8, 65536, 74)
+    flat = s.reshape(-1, 4096)
+    flat[::32] += 3.0
+    assert _retain_large(s, 100, s.size // 4) == (1, 1)
+
+
+def test_topm_sample_unsure():
+    """Two values only, 1.0 on a quarter of the elements (at random) and 0.5
+    elsewhere, budget = the count of ones + the rows: the threshold sits on
+    the edge of the ones' bucket, inside the sample's error, so the sample
+    names nothing and the exact first digit runs."""
+    rng = np.random.default_rng(75)
+    L, H, N = 8, 8, 65536
+    s = np.where(rng.random((L, H, N)) < 0.25, 1.0, 0.5).astype(np.float32)
+    cur = 9
+    ones = int((np.delete(s, cur, axis=2) == 1.0).sum())
+    assert _retain_large(s, cur, ones + L * H) == (0, 1)
+
+
+def test_topm_sample_all_equal():
+    """4M equal scores: one bucket holds every candidate; the sample names it,
+    the split pass lists the whole array and the index order decides."""
+    s = np.full((4, 16, 65536), -2.25, dtype=np.float32)
+    assert _retain_large(s, 0, s.size // 3) == (1, 0)

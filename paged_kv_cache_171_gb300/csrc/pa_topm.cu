@@ -73,6 +73,19 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return ~u;                                        // descending
 }
 
+// A score s that is a number has key f(s) <= K exactly when s >= key_floor(K):
+// the number whose key is K (f is strictly decreasing on the numbers once -0.0
+// is read as 0.0, which float comparison does too); +NaN when K is below the
+// key of +inf (no number qualifies: every comparison with NaN is false); -inf
+// when K is at least the key of -inf (every number qualifies).  A NaN score
+// compares false with every bound; its key is the largest.
+__device__ __forceinline__ float key_floor(uint32_t K) {
+  if (K < 0x007FFFFFu) return __uint_as_float(0x7FC00000u);
+  if (K >= 0xFF800000u) return __uint_as_float(0xFF800000u);
+  const uint32_t u = ~K;
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
 // Zeroes the three histograms, the per-chunk tie counts and the kept-row
 // counts, sets the state.
 __global__ void __launch_bounds__(kThreads)
@@ -325,6 +338,13 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
   load_run(scores, n, base, sc);
   const int t0 = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
   const int r0 = static_cast<int>(static_cast<unsigned>(base) / static_cast<unsigned>(N)) - row0;
+  // Bucket b1 holds keys [b1 << 21, (b1 + 1) << 21): a score is below it when
+  // s >= lo_s, in it or below when s >= hi_s, by float comparisons instead of
+  // keys.  NaN scores (the largest key) are in b1 only when b1 is the last
+  // bucket, where every number is below it.
+  const float lo_s = b1 == 0u ? __uint_as_float(0x7FC00000u) : key_floor((b1 << kShift1) - 1u);
+  const float hi_s = key_floor(((b1 + 1u) << kShift1) - 1u);
+  const bool last = b1 == static_cast<uint32_t>(kBins1 - 1);
   // bit e (e < 16): element base + e is kept / a candidate; bits 16..: the
   // kept candidates (not current positions) below b1
   uint32_t kbits = 0, cbits = 0;
@@ -337,10 +357,10 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
     if (e1 < static_cast<unsigned>(kPerThread)) cur |= 1u << e1;  // in the next row
 #pragma unroll
     for (int e = 0; e < kPerThread; ++e) {
-      const uint32_t bk = score_key(sc[e]) >> kShift1;
-      kbits |= static_cast<uint32_t>(bk < b1) << e;
-      cbits |= static_cast<uint32_t>(bk == b1) << e;
+      kbits |= static_cast<uint32_t>(sc[e] >= lo_s) << e;
+      cbits |= static_cast<uint32_t>(sc[e] >= hi_s) << e;
     }
+    cbits = (last ? (1u << kPerThread) - 1u : cbits) & ~kbits;
     cbits = (cbits & ~cur) | static_cast<uint32_t>(__popc(kbits & ~cur)) << kPerThread;
     kbits |= cur;
     uint4 w;  // bit e of kbits -> byte e
@@ -362,10 +382,10 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
 #pragma unroll
     for (int e = 0; e < kPerThread; ++e) {
       if (base + e >= n) break;
-      const uint32_t bk = score_key(sc[e]) >> kShift1;
-      const bool k = t == current || bk < b1;
-      if (t != current && bk == b1) cbits |= 1u << e;
-      if (t != current && bk < b1) cbits += 1u << kPerThread;
+      const bool below = sc[e] >= lo_s, in = !below && (last || sc[e] >= hi_s);
+      const bool k = t == current || below;
+      if (t != current && in) cbits |= 1u << e;
+      if (t != current && below) cbits += 1u << kPerThread;
       kbits |= static_cast<uint32_t>(k) << e;
       keep[base + e] = k ? 1u : 0u;
       if (per_head && k) {

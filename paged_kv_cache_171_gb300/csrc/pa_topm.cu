@@ -45,6 +45,27 @@ constexpr int kBins1 = 2048, kBins2 = 2048, kBins3 = 1024;  // digits of 11, 11,
 constexpr int kShift1 = 21, kShift2 = 10;
 constexpr int kSampleStep = 32;  // the first-digit sample: every 32nd chunk
 
+// Division by the row length N (tokens per (layer, head)) for dividends below
+// 2^31 by a multiply and a shift -- division by an invariant integer
+// (Granlund and Montgomery, 1994): with s = ceil(log2 N) and
+// M = ceil(2^(31+s) / N) < 2^32, floor(x / N) = floor(x M / 2^(31+s)) for every
+// x < 2^31, since x (M - 2^(31+s)/N) / 2^(31+s) < 2^-s <= 1/N.
+struct RowDiv {
+  int N;
+  uint32_t M, sh;
+  __device__ __forceinline__ int div(int x) const {
+    return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(x)) * M) >> sh);
+  }
+};
+
+RowDiv make_rowdiv(int N) {
+  uint32_t s = 0;
+  while ((static_cast<int64_t>(1) << s) < N) ++s;
+  const uint64_t p = static_cast<uint64_t>(1) << (31 + s);
+  return RowDiv{N, static_cast<uint32_t>((p + static_cast<uint64_t>(N) - 1) / static_cast<uint64_t>(N)),
+                31 + s};
+}
+
 // The state of the select, in the workspace after the histograms.
 struct TopmState {
   uint32_t prefix;     // key bits decided so far (S* at the end)
@@ -157,9 +178,10 @@ __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v) {
 // the sampled b1 (every CTA decides alike from fields no kernel of this step
 // writes; CTA 0 records it, and the remaining rank when confirmed).
 __global__ void __launch_bounds__(kThreads)
-    topm_hist1_kernel(const float *__restrict__ scores, int n, int N, int current,
+    topm_hist1_kernel(const float *__restrict__ scores, int n, RowDiv rd, int current,
                       uint32_t *__restrict__ hist, int step, TopmState *__restrict__ st,
                       int gated) {
+  const int N = rd.N;
   griddep_wait();  // the previous launch of the stream has completed
   griddep_release();
   if (gated) {
@@ -187,7 +209,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = 0; e < kPerThread; ++e) sc[e] = nx[e];
     if (cbase + stride < n)
       load_run(scores, n, static_cast<int>(cbase + stride) + threadIdx.x * kPerThread, nx);
-    const int t0 = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
+    const int t0 = base - rd.div(base) * N;
     uint32_t skip;  // elements that are a current position or past the array
     if (base + kPerThread <= n && N >= kPerThread) {
       skip = 0;
@@ -316,7 +338,7 @@ __global__ void __launch_bounds__(1024)
 // (layer, head) are summed in shared memory, then added once per CTA; so are
 // the kept elements of buckets below b1 (current positions excepted), in the
 // high word of the same 64-bit atomic that reserves the CTA's candidate slots.
-__device__ __forceinline__ void split_chunk(const float *__restrict__ scores, int n, int N,
+__device__ __forceinline__ void split_chunk(const float *__restrict__ scores, int n, RowDiv rd,
                                             int current, uint32_t b1, int cbase,
                                             TopmState *__restrict__ st,
                                             uint8_t *__restrict__ keep,
@@ -325,10 +347,10 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
                                             uint32_t *__restrict__ ckey) {
   __shared__ int cnt[kChunk + 2];  // rows of this chunk, relative to its first
   __shared__ uint32_t wsum[kThreads / 32 + 1], wbel[kThreads / 32];
-  const int row0 = static_cast<int>(static_cast<unsigned>(cbase) / static_cast<unsigned>(N));
+  const int N = rd.N;
+  const int row0 = rd.div(cbase);
   const int cend = min(n, cbase + kChunk);
-  const int n_rows =
-      static_cast<int>(static_cast<unsigned>(cend - 1) / static_cast<unsigned>(N)) - row0 + 1;
+  const int n_rows = rd.div(cend - 1) - row0 + 1;
   if (per_head) {
     for (int i = threadIdx.x; i < n_rows; i += kThreads) cnt[i] = 0;
     __syncthreads();
@@ -336,8 +358,8 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
   const int base = cbase + threadIdx.x * kPerThread;
   float sc[kPerThread];
   load_run(scores, n, base, sc);
-  const int t0 = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
-  const int r0 = static_cast<int>(static_cast<unsigned>(base) / static_cast<unsigned>(N)) - row0;
+  const int rb = rd.div(base);
+  const int t0 = base - rb * N, r0 = rb - row0;
   // Bucket b1 holds keys [b1 << 21, (b1 + 1) << 21): a score is below it when
   // s >= lo_s, in it or below when s >= hi_s, by float comparisons instead of
   // keys.  NaN scores (the largest key) are in b1 only when b1 is the last
@@ -450,14 +472,14 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
 // The split pass, one CTA per chunk.  gate 0: always; 1: on the sampled b1,
 // if the sample named one.
 __global__ void __launch_bounds__(kThreads, 8)
-    topm_split_kernel(const float *__restrict__ scores, int n, int N, int current,
+    topm_split_kernel(const float *__restrict__ scores, int n, RowDiv rd, int current,
                       TopmState *__restrict__ st, uint8_t *__restrict__ keep,
                       int32_t *__restrict__ per_head, uint32_t *__restrict__ cand,
                       uint32_t *__restrict__ ckey, int gate) {
   griddep_wait();  // the previous launch of the stream has completed
   griddep_release();
   if (gate == 1 && !st->sure) return;
-  split_chunk(scores, n, N, current, st->prefix >> kShift1, blockIdx.x * kChunk, st, keep,
+  split_chunk(scores, n, rd, current, st->prefix >> kShift1, blockIdx.x * kChunk, st, keep,
               per_head, cand, ckey);
 }
 
@@ -465,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 8)
 // a grid-stride loop over the chunks, so that the usual case (nothing to do)
 // costs a small grid.
 __global__ void __launch_bounds__(kThreads, 8)
-    topm_split_redo_kernel(const float *__restrict__ scores, int n, int N, int current,
+    topm_split_redo_kernel(const float *__restrict__ scores, int n, RowDiv rd, int current,
                            TopmState *__restrict__ st, uint8_t *__restrict__ keep,
                            int32_t *__restrict__ per_head, uint32_t *__restrict__ cand,
                            uint32_t *__restrict__ ckey) {
@@ -475,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 8)
   const uint32_t b1 = st->prefix >> kShift1;
   for (int64_t cbase = static_cast<int64_t>(blockIdx.x) * kChunk; cbase < n;
        cbase += static_cast<int64_t>(gridDim.x) * kChunk) {
-    split_chunk(scores, n, N, current, b1, static_cast<int>(cbase), st, keep, per_head, cand,
+    split_chunk(scores, n, rd, current, b1, static_cast<int>(cbase), st, keep, per_head, cand,
                 ckey);
     __syncthreads();  // the shared counts are reused by the next chunk
   }
@@ -557,7 +579,7 @@ __global__ void __launch_bounds__(kThreads)
 // The kept candidates: (key, index) <= (S*, idx*).
 __global__ void __launch_bounds__(kThreads)
     topm_cand_keep_kernel(const uint32_t *__restrict__ cand, const uint32_t *__restrict__ ckey,
-                          const TopmState *__restrict__ st, int N, uint8_t *__restrict__ keep,
+                          const TopmState *__restrict__ st, RowDiv rd, uint8_t *__restrict__ keep,
                           int32_t *__restrict__ per_head) {
   griddep_wait();  // the previous launch of the stream has completed
   griddep_release();
@@ -566,8 +588,7 @@ __global__ void __launch_bounds__(kThreads)
     const bool kept = valid && (k < skey || (k == skey && idx <= istar));
     if (kept) keep[idx] = 1;
     if (per_head)
-      warp_add(reinterpret_cast<uint32_t *>(per_head),
-               static_cast<int>(idx / static_cast<uint32_t>(N)), kept);
+      warp_add(reinterpret_cast<uint32_t *>(per_head), rd.div(static_cast<int>(idx)), kept);
   });
 }
 
@@ -645,23 +666,24 @@ __global__ void __launch_bounds__(kThreads)
 // current positions; true: every element.  Kept rows per (layer, head) are
 // summed in shared memory, then added once per CTA.
 __global__ void __launch_bounds__(kThreads)
-    topm_mask_kernel(int n, int N, int current, bool all, uint8_t *__restrict__ keep,
+    topm_mask_kernel(int n, RowDiv rd, int current, bool all, uint8_t *__restrict__ keep,
                      int32_t *__restrict__ per_head) {
+  const int N = rd.N;
   griddep_wait();  // the previous launch of the stream has completed
   griddep_release();
   __shared__ int cnt[kChunk + 2];  // rows of this chunk, relative to its first
   const int cbase = blockIdx.x * kChunk;
-  const int row0 = static_cast<int>(static_cast<unsigned>(cbase) / static_cast<unsigned>(N));
+  const int row0 = rd.div(cbase);
   const int cend = min(n, cbase + kChunk);
-  const int n_rows =
-      static_cast<int>(static_cast<unsigned>(cend - 1) / static_cast<unsigned>(N)) - row0 + 1;
+  const int n_rows = rd.div(cend - 1) - row0 + 1;
   if (per_head) {
     for (int i = threadIdx.x; i < n_rows; i += kThreads) cnt[i] = 0;
     __syncthreads();
   }
   const int base = cbase + threadIdx.x * kPerThread;
-  int t = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
-  int row = static_cast<int>(static_cast<unsigned>(base) / static_cast<unsigned>(N)) - row0;
+  int row = rd.div(base);
+  int t = base - row * N;
+  row -= row0;
   int run_row = -1, run = 0;  // kept count of the current (layer, head) run
   uint32_t bytes[kPerThread / 4] = {0u, 0u, 0u, 0u};
 #pragma unroll
@@ -746,11 +768,12 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
   const int64_t k = budget - static_cast<int64_t>(n_layers) * n_heads;  // candidates kept
   const int mode = k <= 0 ? 0 : (k >= n_cand ? 1 : 2);
   const int ni = static_cast<int>(n);
+  const RowDiv rd = make_rowdiv(n_tokens);
   if (mode != 2) {
     if (kept_per_head &&
         cudaMemsetAsync(kept_per_head, 0, sizeof(int32_t) * n_layers * n_heads, s) != cudaSuccess)
       return PA_ERR_CUDA;
-    topm_mask_kernel<<<n_chunks, kThreads, 0, s>>>(ni, n_tokens, current, mode == 1, keep,
+    topm_mask_kernel<<<n_chunks, kThreads, 0, s>>>(ni, rd, current, mode == 1, keep,
                                                    kept_per_head);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
@@ -773,32 +796,32 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
     const int n_sampled = (n_chunks + kSampleStep - 1) / kSampleStep;
     const int sgrid = n_sampled < sms * 4 ? n_sampled : sms * 4;
     if (e == cudaSuccess)
-      e = launch_pdl(topm_hist1_kernel, dim3(sgrid), T, 0, s, scores, ni, n_tokens, current,
+      e = launch_pdl(topm_hist1_kernel, dim3(sgrid), T, 0, s, scores, ni, rd, current,
                      hist1, kSampleStep, st, 0);
     if (e == cudaSuccess)
       e = launch_pdl(topm_pick_sample_kernel, one, T1k, 0, s, hist1, st,
                      static_cast<float>(n_cand));
     if (e == cudaSuccess)
-      e = launch_pdl(topm_split_kernel, dim3(n_chunks), T, 0, s, scores, ni, n_tokens, current,
+      e = launch_pdl(topm_split_kernel, dim3(n_chunks), T, 0, s, scores, ni, rd, current,
                      st, keep, kept_per_head, cand, ckey, 1);
     if (e == cudaSuccess)
-      e = launch_pdl(topm_hist1_kernel, dim3(grid), T, 0, s, scores, ni, n_tokens, current,
+      e = launch_pdl(topm_hist1_kernel, dim3(grid), T, 0, s, scores, ni, rd, current,
                      hist1, 1, st, 1);
     if (e == cudaSuccess)
       e = launch_pdl(topm_pick_kernel<kBins1>, one, T1k, 0, s, hist1, st, kShift1, 1,
                      kept_per_head, n_rows);
     if (e == cudaSuccess)
-      e = launch_pdl(topm_split_redo_kernel, dim3(grid), T, 0, s, scores, ni, n_tokens, current,
+      e = launch_pdl(topm_split_redo_kernel, dim3(grid), T, 0, s, scores, ni, rd, current,
                      st, keep, kept_per_head, cand, ckey);
   } else {
     if (e == cudaSuccess)
-      e = launch_pdl(topm_hist1_kernel, dim3(grid), T, 0, s, scores, ni, n_tokens, current,
+      e = launch_pdl(topm_hist1_kernel, dim3(grid), T, 0, s, scores, ni, rd, current,
                      hist1, 1, st, 0);
     if (e == cudaSuccess)
       e = launch_pdl(topm_pick_kernel<kBins1>, one, T1k, 0, s, hist1, st, kShift1, 0, no_rows,
                      0);
     if (e == cudaSuccess)
-      e = launch_pdl(topm_split_kernel, dim3(n_chunks), T, 0, s, scores, ni, n_tokens, current,
+      e = launch_pdl(topm_split_kernel, dim3(n_chunks), T, 0, s, scores, ni, rd, current,
                      st, keep, kept_per_head, cand, ckey, 0);
   }
   if (e == cudaSuccess)
@@ -815,7 +838,7 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
   if (e == cudaSuccess)
     e = launch_pdl(topm_tiefind_kernel, one, T, 0, s, scores, ni, n_tokens, current, st);
   if (e == cudaSuccess)
-    e = launch_pdl(topm_cand_keep_kernel, dim3(cgrid), T, 0, s, cand, ckey, st, n_tokens, keep,
+    e = launch_pdl(topm_cand_keep_kernel, dim3(cgrid), T, 0, s, cand, ckey, st, rd, keep,
                    kept_per_head);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -592,13 +592,17 @@ __global__ void __launch_bounds__(kThreads)
   });
 }
 
-// One CTA of 1024 threads: the chunk holding the k_rem-th tie, from an
-// exclusive scan of the chunk tie counts (each thread first sums a run).
+// One CTA of 1024 threads: the last kept candidate.  First the chunk holding
+// the k_rem-th tie (candidate with key S*), from an exclusive scan of the
+// chunk tie counts (each thread first sums a run); then that tie's index
+// idx*, ranking the chunk's ties in index order (four elements a thread).
 __global__ void __launch_bounds__(1024)
-    topm_scan_kernel(const uint32_t *__restrict__ tiecnt, int n_chunks,
-                     TopmState *__restrict__ st) {
+    topm_tierank_kernel(const uint32_t *__restrict__ tiecnt, int n_chunks,
+                        const float *__restrict__ scores, int n, RowDiv rd, int current,
+                        TopmState *__restrict__ st) {
   griddep_wait();  // the previous launch of the stream has completed
   griddep_release();
+  __shared__ uint32_t s_chunk, s_rank;
   // runs of a multiple of 4 counts, loaded 16 bytes at a time (the counts
   // start 16-byte aligned)
   const int per = ((n_chunks + 1023) / 1024 + 3) & ~3;
@@ -614,7 +618,8 @@ __global__ void __launch_bounds__(1024)
     const uint4 v = quad(i);
     sum += v.x + v.y + v.z + v.w;
   }
-  const uint32_t r = st->k_rem;
+  const uint32_t r = st->k_rem, skey = st->prefix;
+  if (threadIdx.x == 0) s_chunk = s_rank = 0u;  // (rank 0: no index; cannot happen)
   uint32_t run = block_scan_incl<1024>(sum) - sum;
   if (run < r && r <= run + sum) {  // exactly one thread
     for (int i = lo; i < hi; i += 4) {
@@ -624,8 +629,8 @@ __global__ void __launch_bounds__(1024)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (!found && run < r && r <= run + v[u]) {
-          st->tie_chunk = static_cast<uint32_t>(i + u);
-          st->tie_rank = r - run;
+          s_chunk = st->tie_chunk = static_cast<uint32_t>(i + u);
+          s_rank = st->tie_rank = r - run;
           found = true;
         }
         if (!found) run += v[u];
@@ -633,28 +638,19 @@ __global__ void __launch_bounds__(1024)
       if (found) break;
     }
   }
-}
-
-// One CTA: the index of the tie_rank-th candidate with key S* inside chunk
-// tie_chunk (index order).
-__global__ void __launch_bounds__(kThreads)
-    topm_tiefind_kernel(const float *__restrict__ scores, int n, int N, int current,
-                        TopmState *__restrict__ st) {
-  griddep_wait();  // the previous launch of the stream has completed
-  griddep_release();
-  const uint32_t skey = st->prefix, want = st->tie_rank;
-  const int base = static_cast<int>(st->tie_chunk) * kChunk + threadIdx.x * kPerThread;
-  float sc[kPerThread];
-  load_run(scores, n, base, sc);
-  int t = static_cast<int>(static_cast<unsigned>(base) % static_cast<unsigned>(N));
+  __syncthreads();  // also ends every thread's use of the scan's shared totals
+  const uint32_t want = s_rank;
+  const int base = static_cast<int>(s_chunk) * kChunk + threadIdx.x * 4;
   uint32_t tie_bits = 0;  // bit e: element base + e is a tie
+  int t = base - rd.div(base) * rd.N;
 #pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    if (base + e < n && t != current && score_key(sc[e]) == skey) tie_bits |= 1u << e;
-    if (++t == N) t = 0;
+  for (int e = 0; e < 4; ++e) {
+    if (base + e < n && t != current && score_key(__ldg(scores + base + e)) == skey)
+      tie_bits |= 1u << e;
+    if (++t == rd.N) t = 0;
   }
   const uint32_t ties = __popc(tie_bits);
-  const uint32_t before = block_scan_incl<kThreads>(ties) - ties;
+  const uint32_t before = block_scan_incl<1024>(ties) - ties;
   if (before < want && want <= before + ties) {  // exactly one thread
     uint32_t bits = tie_bits;
     for (uint32_t k = before + 1; k < want; ++k) bits &= bits - 1;  // drop earlier ties
@@ -834,9 +830,9 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
     e = launch_pdl(topm_pick_kernel<kBins3>, one, T1k, 0, s, hist3, st, 0, 0, no_rows, 0);
   if (e == cudaSuccess)
     e = launch_pdl(topm_cand_tie_kernel, dim3(cgrid), T, 0, s, cand, ckey, st, tiecnt);
-  if (e == cudaSuccess) e = launch_pdl(topm_scan_kernel, one, T1k, 0, s, tiecnt, n_chunks, st);
   if (e == cudaSuccess)
-    e = launch_pdl(topm_tiefind_kernel, one, T, 0, s, scores, ni, n_tokens, current, st);
+    e = launch_pdl(topm_tierank_kernel, one, T1k, 0, s, tiecnt, n_chunks, scores, ni, rd, current,
+                   st);
   if (e == cudaSuccess)
     e = launch_pdl(topm_cand_keep_kernel, dim3(cgrid), T, 0, s, cand, ckey, st, rd, keep,
                    kept_per_head);

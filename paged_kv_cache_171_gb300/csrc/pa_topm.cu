@@ -338,6 +338,10 @@ __global__ void __launch_bounds__(1024)
 // (layer, head) are summed in shared memory, then added once per CTA; so are
 // the kept elements of buckets below b1 (current positions excepted), in the
 // high word of the same 64-bit atomic that reserves the CTA's candidate slots.
+// LONG (rows of at least kChunk tokens): a chunk meets at most two rows, so
+// each warp sums its kept counts of the two by shuffles and the CTA adds them
+// from the warp totals -- no shared counters to clear or contend on.
+template <bool LONG>
 __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, int n, RowDiv rd,
                                             int current, uint32_t b1, int cbase,
                                             TopmState *__restrict__ st,
@@ -345,13 +349,13 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
                                             int32_t *__restrict__ per_head,
                                             uint32_t *__restrict__ cand,
                                             uint32_t *__restrict__ ckey) {
-  __shared__ int cnt[kChunk + 2];  // rows of this chunk, relative to its first
-  __shared__ uint32_t wsum[kThreads / 32 + 1], wbel[kThreads / 32];
+  __shared__ int cnt[LONG ? 1 : kChunk + 2];  // rows of this chunk, relative to its first
+  __shared__ uint32_t wsum[kThreads / 32 + 1], wbel[kThreads / 32], wrow[2][kThreads / 32];
   const int N = rd.N;
   const int row0 = rd.div(cbase);
   const int cend = min(n, cbase + kChunk);
   const int n_rows = rd.div(cend - 1) - row0 + 1;
-  if (per_head) {
+  if (!LONG && per_head) {
     for (int i = threadIdx.x; i < n_rows; i += kThreads) cnt[i] = 0;
     __syncthreads();
   }
@@ -391,7 +395,7 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
     w.z = (((kbits >> 8) & 15u) * 0x00204081u) & 0x01010101u;
     w.w = (((kbits >> 12) & 15u) * 0x00204081u) & 0x01010101u;
     *reinterpret_cast<uint4 *>(keep + base) = w;
-    if (per_head) {
+    if (!LONG && per_head) {
       const int split = N - t0 < kPerThread ? N - t0 : kPerThread;  // elements in row r0
       const uint32_t lo = kbits & ((1u << split) - 1u), hi = kbits >> split;
       if (lo) atomicAdd(&cnt[r0], __popc(lo));
@@ -410,7 +414,7 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
       if (t != current && below) cbits += 1u << kPerThread;
       kbits |= static_cast<uint32_t>(k) << e;
       keep[base + e] = k ? 1u : 0u;
-      if (per_head && k) {
+      if (!LONG && per_head && k) {
         if (row != run_row) {
           if (run) atomicAdd(&cnt[run_row], run);
           run_row = row;
@@ -423,7 +427,18 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
         ++row;
       }
     }
-    if (per_head && run) atomicAdd(&cnt[run_row], run);
+    if (!LONG && per_head && run) atomicAdd(&cnt[run_row], run);
+  }
+  if (LONG && per_head) {  // kept counts of rows row0 and row0 + 1, per warp
+    const int64_t in0 = static_cast<int64_t>(row0 + 1) * N - base;  // this run's in row0
+    const uint32_t m0 =
+        in0 >= kPerThread ? 0xFFFFu : (in0 <= 0 ? 0u : (1u << static_cast<int>(in0)) - 1u);
+    const uint32_t c0 = __reduce_add_sync(0xffffffffu, __popc(kbits & m0));
+    const uint32_t c1 = __reduce_add_sync(0xffffffffu, __popc(kbits & ~m0));
+    if ((threadIdx.x & 31) == 0) {
+      wrow[0][threadIdx.x >> 5] = c0;
+      wrow[1][threadIdx.x >> 5] = c1;
+    }
   }
   // append the candidates in index order and add the kept-below count: one
   // 64-bit atomic per CTA (candidates in the low word, which cannot carry)
@@ -463,7 +478,14 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
     cand[pos] = static_cast<uint32_t>(i);
     ckey[pos++] = score_key(__ldg(scores + i));
   }
-  if (per_head) {
+  if (LONG) {
+    if (per_head && threadIdx.x < 64) {  // warp 0: row0, warp 1: row0 + 1
+      const int r = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      const uint32_t c =
+          __reduce_add_sync(0xffffffffu, lane < kThreads / 32 ? wrow[r][lane] : 0u);
+      if (lane == 0 && c) atomicAdd(per_head + row0 + r, static_cast<int>(c));
+    }
+  } else if (per_head) {
     for (int i = threadIdx.x; i < n_rows; i += kThreads)
       if (cnt[i]) atomicAdd(per_head + row0 + i, cnt[i]);
   }
@@ -471,6 +493,7 @@ __device__ __forceinline__ void split_chunk(const float *__restrict__ scores, in
 
 // The split pass, one CTA per chunk.  gate 0: always; 1: on the sampled b1,
 // if the sample named one.
+template <bool LONG>
 __global__ void __launch_bounds__(kThreads, 8)
     topm_split_kernel(const float *__restrict__ scores, int n, RowDiv rd, int current,
                       TopmState *__restrict__ st, uint8_t *__restrict__ keep,
@@ -479,13 +502,14 @@ __global__ void __launch_bounds__(kThreads, 8)
   griddep_wait();  // the previous launch of the stream has completed
   griddep_release();
   if (gate == 1 && !st->sure) return;
-  split_chunk(scores, n, rd, current, st->prefix >> kShift1, blockIdx.x * kChunk, st, keep,
+  split_chunk<LONG>(scores, n, rd, current, st->prefix >> kShift1, blockIdx.x * kChunk, st, keep,
               per_head, cand, ckey);
 }
 
 // The split pass on the exact b1, only if the sampled one was not confirmed:
 // a grid-stride loop over the chunks, so that the usual case (nothing to do)
 // costs a small grid.
+template <bool LONG>
 __global__ void __launch_bounds__(kThreads, 8)
     topm_split_redo_kernel(const float *__restrict__ scores, int n, RowDiv rd, int current,
                            TopmState *__restrict__ st, uint8_t *__restrict__ keep,
@@ -497,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 8)
   const uint32_t b1 = st->prefix >> kShift1;
   for (int64_t cbase = static_cast<int64_t>(blockIdx.x) * kChunk; cbase < n;
        cbase += static_cast<int64_t>(gridDim.x) * kChunk) {
-    split_chunk(scores, n, rd, current, b1, static_cast<int>(cbase), st, keep, per_head, cand,
+    split_chunk<LONG>(scores, n, rd, current, b1, static_cast<int>(cbase), st, keep, per_head, cand,
                 ckey);
     __syncthreads();  // the shared counts are reused by the next chunk
   }
@@ -787,6 +811,9 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
   cudaError_t e = launch_pdl(topm_init_kernel, dim3(sms), T, 0, s, hist1, n_zero, tiecnt,
                              n_chunks, kept_per_head, n_rows, st, static_cast<uint32_t>(k));
   int32_t *const no_rows = nullptr;
+  const bool long_rows = n_tokens >= kChunk;  // a chunk meets at most two rows
+  auto split = long_rows ? topm_split_kernel<true> : topm_split_kernel<false>;
+  auto split_redo = long_rows ? topm_split_redo_kernel<true> : topm_split_redo_kernel<false>;
   if (n_chunks >= kSampleStep * 16) {
     // the sampled first digit; the exact one behind it, gated on the counts
     const int n_sampled = (n_chunks + kSampleStep - 1) / kSampleStep;
@@ -798,7 +825,7 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
       e = launch_pdl(topm_pick_sample_kernel, one, T1k, 0, s, hist1, st,
                      static_cast<float>(n_cand));
     if (e == cudaSuccess)
-      e = launch_pdl(topm_split_kernel, dim3(n_chunks), T, 0, s, scores, ni, rd, current,
+      e = launch_pdl(split, dim3(n_chunks), T, 0, s, scores, ni, rd, current,
                      st, keep, kept_per_head, cand, ckey, 1);
     if (e == cudaSuccess)
       e = launch_pdl(topm_hist1_kernel, dim3(grid), T, 0, s, scores, ni, rd, current,
@@ -807,7 +834,7 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
       e = launch_pdl(topm_pick_kernel<kBins1>, one, T1k, 0, s, hist1, st, kShift1, 1,
                      kept_per_head, n_rows);
     if (e == cudaSuccess)
-      e = launch_pdl(topm_split_redo_kernel, dim3(grid), T, 0, s, scores, ni, rd, current,
+      e = launch_pdl(split_redo, dim3(grid), T, 0, s, scores, ni, rd, current,
                      st, keep, kept_per_head, cand, ckey);
   } else {
     if (e == cudaSuccess)
@@ -817,7 +844,7 @@ int pa_topm_retain(const float *scores, int n_layers, int n_heads, int n_tokens,
       e = launch_pdl(topm_pick_kernel<kBins1>, one, T1k, 0, s, hist1, st, kShift1, 0, no_rows,
                      0);
     if (e == cudaSuccess)
-      e = launch_pdl(topm_split_kernel, dim3(n_chunks), T, 0, s, scores, ni, rd, current,
+      e = launch_pdl(split, dim3(n_chunks), T, 0, s, scores, ni, rd, current,
                      st, keep, kept_per_head, cand, ckey, 0);
   }
   if (e == cudaSuccess)

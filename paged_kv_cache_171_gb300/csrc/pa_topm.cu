@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 8)
 // Counts go through warp-aggregated atomics: the lanes that share a target
 // (a bin, a chunk, a row) elect one to add their number, which keeps heavily
 // tied scores from serializing on one address.
-constexpr int kCandPer = 4;
+constexpr int kCandPer = 8;
 
 __device__ __forceinline__ void warp_add(uint32_t *addr_base, int slot, bool on, uint32_t n = 1) {
   const unsigned act = __ballot_sync(0xffffffffu, on);

@@ -66,7 +66,10 @@ RowDiv make_rowdiv(int N) {
                 31 + s};
 }
 
-// The state of the select, in the workspace after the histograms.
+// The state of the select, in the workspace after the histograms (128-byte
+// aligned).  The split pass's counters sit in a cache line of their own: every
+// split CTA reads b1 from the first line, and an atomic on that line would
+// evict the copies the SMs' L1 caches hold.
 struct TopmState {
   uint32_t prefix;     // key bits decided so far (S* at the end)
   uint32_t mask;       // which bits are decided
@@ -74,14 +77,20 @@ struct TopmState {
   uint32_t tie_chunk;  // chunk holding the k_rem-th candidate with key S*
   uint32_t tie_rank;   // its 1-based rank among that chunk's ties
   uint32_t idx_star;   // its index: the last kept candidate
-  uint32_t n_cand;     // elements of bucket b1 appended to the candidate list
-  uint32_t kept_below; // kept candidates of buckets below b1 (the split pass)
+  uint32_t pad0[2];
   uint32_t sure;       // 1: b1 named by the sample (the split pass ran on it)
   uint32_t redo;       // 1: b1 not confirmed; the exact first digit runs
   uint32_t k_total;    // K, the candidates to keep
-  uint32_t pad;
+  uint32_t pad1[21];
+  uint32_t n_cand;     // elements of bucket b1 appended to the candidate list
+  uint32_t kept_below; // kept candidates of buckets below b1 (the split pass)
+  uint32_t pad2[30];
 };
-static_assert(sizeof(TopmState) % 16 == 0, "the tie counts follow, 16-byte aligned");
+static_assert(sizeof(TopmState) == 256 && offsetof(TopmState, n_cand) == 128,
+              "two cache lines, the counters in the second");
+static_assert(offsetof(TopmState, kept_below) == offsetof(TopmState, n_cand) + 4,
+              "n_cand and kept_below are the low and high words of one 64-bit counter");
+static_assert((kBins1 + kBins2 + kBins3) * 4 % 128 == 0, "the state starts a cache line");
 static_assert(offsetof(TopmState, n_cand) % 8 == 0 &&
                   offsetof(TopmState, kept_below) == offsetof(TopmState, n_cand) + 4,
               "n_cand and kept_below are the low and high words of one 64-bit counter");
@@ -120,8 +129,11 @@ __global__ void __launch_bounds__(kThreads)
   for (int i = blockIdx.x * kThreads + threadIdx.x; i < n_chunks; i += stride) tiecnt[i] = 0;
   if (per_head)
     for (int i = blockIdx.x * kThreads + threadIdx.x; i < n_rows; i += stride) per_head[i] = 0;
-  if (blockIdx.x == 0 && threadIdx.x == 0)
-    *st = TopmState{0u, 0u, k, 0u, 0u, 0u, 0u, 0u, 0u, 0u, k, 0u};
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    TopmState z = {};
+    z.k_rem = z.k_total = k;
+    *st = z;
+  }
 }
 
 // The kPerThread consecutive scores from `base` (16-byte aligned when the

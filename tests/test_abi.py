@@ -244,7 +244,7 @@ def test_topm_arguments(L):
     P = FAKE
     ws = L.pa_topm_workspace_size(32, 32, 32768)
     n = 32 * 32 * 32768
-    head = (2048 + 2048 + 1024) * 4 + 48 + -(-n // 4096) * 4  # histograms, state, tie counts
+    head = (2048 + 2048 + 1024) * 4 + 256 + -(-n // 4096) * 4  # histograms, state, tie counts
     assert ws == -(-head // 16) * 16 + 8 * n                   # + a candidate (index, key) per element
     assert L.pa_topm_workspace_size(0, 1, 1) == 0
     r = L.pa_topm_retain

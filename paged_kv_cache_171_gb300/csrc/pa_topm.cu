@@ -28,9 +28,10 @@
 // sample unsure, or wrong) the exact first digit runs: a histogram over every
 // element, its pick, and the split pass again.  Arrays under 512 chunks take
 // the exact first digit directly.  The remaining digits, the tie rank and the
-// final keeps then run over the candidates alone: the r-th tie is located by counting ties per chunk of the array, scanning
-// the counts to find its chunk, and ranking that one chunk's ties; with its
-// index idx*, a candidate is kept when (f, index) <= (S*, idx*).
+// final keeps then run over the candidates alone: the r-th tie is located by
+// counting ties per chunk of the array, then (one launch) scanning the counts
+// to find its chunk and ranking that one chunk's ties; with its index idx*, a
+// candidate is kept when (f, index) <= (S*, idx*).
 #include "pa_device.cuh"
 #include "pa_internal.h"
 

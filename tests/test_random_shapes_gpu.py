@@ -170,3 +170,40 @@ def test_random_cascade(seed):
     assert_close(out.cpu().numpy(), ref,
                  f"cascade B={B} {hq}/{hkv} D={D} {dtype} prefix {prefix_len} own {own} part {part}")
     assert pa.pa_last_device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_topm(seed):
+    """Budgeted top-M retention on seeded random shapes: row lengths on both
+    sides of 4096 (short rows sum per-row counts in shared memory, long rows
+    per warp), arrays on both sides of 2M scores (the sampled first digit),
+    coarse and fine score grids, any current position and budget; the kept
+    set is unique, so masks and per-row counts must equal the oracle's."""
+    rng = np.random.default_rng(7400 + seed)
+    N = int(rng.choice([int(rng.integers(1, 4096)), int(rng.integers(4096, 70000)),
+                        4095, 4096, 4097]))
+    if seed % 3 == 0:  # 2.2M-4.5M scores: the sampled first digit
+        rows = -(-int(rng.integers(2_200_000, 4_500_000)) // N)
+        L = int(rng.integers(1, 9))
+        H = -(-rows // L)
+    else:
+        L = int(rng.integers(1, 9))
+        H = int(rng.integers(1, 9))
+    n = L * H * N
+    s = rng.standard_normal((L, H, N)).astype(np.float32)
+    grid = rng.choice([0, 2, 16, 256])
+    if grid:
+        s = (np.round(s * grid) / grid).astype(np.float32)
+    current = int(rng.integers(0, N))
+    budgets = {int(rng.integers(0, n + 10)), L * H + int(rng.integers(1, max(2, n // 4))),
+               n // 4}
+    dev = torch.from_numpy(s).cuda()
+    for budget in sorted(budgets):
+        keep, per_head = pa.topm_retain(dev, current, budget)
+        torch.cuda.synchronize()
+        want = oracle.topm_retain(s, current, budget)
+        got = keep.cpu().numpy().astype(bool)
+        assert np.array_equal(got, want), (L, H, N, current, budget, grid,
+                                           int((got != want).sum()))
+        assert np.array_equal(per_head.cpu().numpy(), want.sum(axis=2)), (L, H, N, budget)
+    assert pa.pa_last_device_error() == 0

@@ -173,7 +173,7 @@ def test_random_cascade(seed):
 
 
 @pytest.mark.parametrize("seed", range(10))
-def test_random_topm(seed):
+def test_random_topm_routes(seed):
     """Budgeted top-M retention on seeded random shapes: row lengths on both
     sides of 4096 (short rows sum per-row counts in shared memory, long rows
     per warp), arrays on both sides of 2M scores (the sampled first digit),
